@@ -1,0 +1,530 @@
+"""Benchmark of the EP dispatch/combine hot path on GB300.
+
+One step = layout -> dispatch -> combine over one batch of the DeepSeek-V3-shaped
+prefill workload (T=4096 tokens, H=7168 bf16, E=256 experts, top-8, R=32
+virtual ranks = 8 nodes x 4), inputs resident in HBM. The expert between
+dispatch and combine is the identity (combine reads the dispatch buffer), so
+no harness work sits in the timed region. L2 is flushed between steps by a
+256 MiB write outside the timed events.
+
+Prints ONE JSON line (rank 0): value = algorithmic HBM GB/s of the step
+(whole job, summed over ranks), plus tokens/s, the roofline of the dominant
+kernel, per-stage times for the other workloads (FP8 dispatch, restripe and
+node dispatch, skewed routing), an end-to-end number through host buffers,
+the CPU oracle as a baseline, and SM clocks sampled during the timed region.
+
+--impl reference times the oracle (plain single-threaded C) on the host on
+the same workload and prints the same line with "impl": "reference".
+
+Multi-GPU (torchrun): each rank runs an independent replica of the workload on
+its own GPU (token batches are independent; no collective on the data path);
+timing is bracketed by barriers and the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "dispatch+combine HBM GB/s & tokens/s at T=4096,H=7168,E=256,k=8; % of HBM peak"
+UNIT = "GB/s"
+FLUSH_BYTES = 256 << 20
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# --------------------------------------------------------------------------- byte accounting
+
+def step_bytes(T, H, k, E, R, N, pairs, row_bytes_out=None):
+    """Algorithmic HBM bytes of each stage (what the method must move).
+
+    pairs = number of (token, rank) deliveries = sum of tokens_per_rank.
+    layout:   read topk_idx T*k*8; write is_token_in_rank T*R, slot 4*T*R,
+              is_token_in_node T*N, counts 4*(E+R+N)
+    dispatch: read x T*2H (+ slot row 4*T*R, topk 12*T*k); write per delivery the row
+              plus src index 4 + topk ids/weights 8k
+    combine:  read one row per delivery + slot 4*T*R; write T*2H
+    """
+    row = 2 * H if row_bytes_out is None else row_bytes_out
+    layout = T * k * 8 + T * R * 5 + T * N + 4 * (E + R + N)
+    dispatch = T * 2 * H + 4 * T * R + 12 * T * k + pairs * (row + 4 + 8 * k)
+    combine = pairs * 2 * H + 4 * T * R + T * 2 * H
+    return {"layout": layout, "dispatch": dispatch, "combine": combine}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(name):
+    path = os.path.join(ROOT, "combine_ep_get_05_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "combine_ep_get_05_gb300", "csrc", "ep_common.cuh")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel, source):
+    """dram read+write bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)
+        e = t.get(kernel)
+        if e and e.get("source_sha") == source_digest(source):
+            return e.get("dram_bytes_per_launch_full"), e.get("note")
+    except Exception:
+        pass
+    return None, None
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            self.uuid = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.uuid and self.uuid.replace("GPU-", "") not in parts[0]:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        try:
+            sm = [float(r[1]) for r in rows]
+            mx = max(float(r[2]) for r in rows)
+        except ValueError:
+            return None
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, value):
+    if world == 1:
+        return value
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- oracle (CPU) timing
+
+def oracle_step_seconds(w, max_tokens, tokens):
+    """One oracle step (layout -> dispatch -> identity combine) on the first `tokens` tokens."""
+    import oracle
+
+    topk = np.ascontiguousarray(w.topk_idx[:tokens])
+    x = np.ascontiguousarray(w.x[:tokens])
+    tw = np.ascontiguousarray(w.topk_w[:tokens])
+    t0 = time.perf_counter()
+    L = oracle.layout(topk, w.E, w.R, w.ranks_per_node)
+    D = oracle.dispatch(x, topk, tw, L["slot"], w.E, w.R, max_tokens)
+    oracle.combine(D["recv_x"], L["slot"], max_tokens)
+    dt = time.perf_counter() - t0
+    return dt, int(L["tokens_per_rank"].sum())
+
+
+def cpu_baseline(w, budget_s=12.0, tokens=None):
+    import oracle
+
+    oracle.build()
+    tokens = tokens or w.T
+    N = w.num_nodes
+    spent, steps, pairs = 0.0, 0, 0
+    while spent < budget_s and steps < 50:
+        dt, pairs = oracle_step_seconds(w, tokens, tokens)
+        spent += dt
+        steps += 1
+    b = step_bytes(tokens, w.H, w.k, w.E, w.R, N, pairs)
+    total = sum(b.values())
+    return {
+        "value": round(total / (spent / steps) / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "sample": f"{steps} oracle steps (layout+dispatch+identity combine) on {tokens} of the {w.T} tokens, "
+                  f"single-threaded C, {spent:.1f} s",
+        "tokens_per_s": round(tokens / (spent / steps), 1),
+    }
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, world, rank):
+    import combine_ep_get_05_gb300 as ep
+
+    ep.build_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = workloads.make("dsv3")
+    T, H, E, k, R, rpn = w.T, w.H, w.E, w.k, w.R, w.ranks_per_node
+    N = w.num_nodes
+    M = w.max_tokens
+    x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(w.topk_idx).to(dev)
+    tw = torch.from_numpy(w.topk_w).to(dev)
+    lay = ep.alloc_layout(T, E, R, rpn, dev)
+    disp = ep.alloc_dispatch(R, M, H, k, fp8=False, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    cstatus = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ep.get_layout(topk, E, R, rpn, out=lay)
+        ep.dispatch(x, topk, tw, lay, M, out=disp)
+        ep.combine(disp.recv_x, lay, M, out=out, status=cstatus)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    pairs = int(lay.tokens_per_rank.sum().item())
+    flags = ep.read_flags(lay.status) | ep.read_flags(disp.status) | ep.read_flags(cstatus)
+    if flags:
+        raise RuntimeError(f"kernels raised status flags {flags}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        e = ev[i]
+        e[0].record(stream)
+        ep.get_layout(topk, E, R, rpn, out=lay)
+        e[1].record(stream)
+        ep.dispatch(x, topk, tw, lay, M, out=disp)
+        e[2].record(stream)
+        ep.combine(disp.recv_x, lay, M, out=out, status=cstatus)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+
+    stage_ms = {"layout": [], "dispatch": [], "combine": []}
+    step_ms = []
+    for e in ev:
+        stage_ms["layout"].append(e[0].elapsed_time(e[1]))
+        stage_ms["dispatch"].append(e[1].elapsed_time(e[2]))
+        stage_ms["combine"].append(e[2].elapsed_time(e[3]))
+        step_ms.append(e[0].elapsed_time(e[3]))
+    ms = max_over_ranks(world, statistics.mean(step_ms))
+    b = step_bytes(T, H, k, E, R, N, pairs)
+    total_bytes = sum(b.values())
+    value = world * total_bytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    mean = {s: statistics.mean(v) for s, v in stage_ms.items()}
+    dom = max(("dispatch", "combine"), key=lambda s: mean[s])
+    dom_kernel = {"dispatch": "dispatch_bf16_kernel", "combine": "combine_kernel"}[dom]
+    dom_src = {"dispatch": "ep_dispatch.cu", "combine": "ep_combine.cu"}[dom]
+    achieved = b[dom] / (mean[dom] * 1e-3) / 1e9
+    traffic, traffic_note = committed_traffic(dom_kernel, dom_src)
+
+    stages = {s: {"ms": round(mean[s], 4), "ms_p10": round(float(np.percentile(stage_ms[s], 10)), 4),
+                  "ms_p90": round(float(np.percentile(stage_ms[s], 90)), 4),
+                  "alg_bytes": b[s], "gbs": round(b[s] / (mean[s] * 1e-3) / 1e9, 1),
+                  "frac_of_hbm_peak": round(b[s] / (mean[s] * 1e-3) / 1e9 / peak, 4)} for s in stage_ms}
+
+    # ----- end to end through the public API with pinned host buffers
+    x_h = torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    topk_h = torch.from_numpy(w.topk_idx).pin_memory()
+    tw_h = torch.from_numpy(w.topk_w).pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    topk_d = torch.empty_like(topk)
+    tw_d = torch.empty_like(tw)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        topk_d.copy_(topk_h, non_blocking=True)
+        tw_d.copy_(tw_h, non_blocking=True)
+        ep.get_layout(topk_d, E, R, rpn, out=lay)
+        ep.dispatch(x_d, topk_d, tw_d, lay, M, out=disp)
+        ep.combine(disp.recv_x, lay, M, out=out, status=cstatus)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        z.record(stream)
+        z.synchronize()
+        e2e_ms.append(a.elapsed_time(z))
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out.cpu())
+    e2e_t = max_over_ranks(world, statistics.mean(e2e_ms))
+    h2d = x_h.numel() * 2 + topk_h.numel() * 8 + tw_h.numel() * 4
+    d2h = out_h.numel() * 2
+
+    extra = {} if args.skip_extra else extra_stages(ep, dev, args, flush, peak)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "dsv3 prefill: T=4096 H=7168 bf16, E=256 top-8, R=32 virtual ranks "
+                               "(8 nodes x 4), max_tokens=4096, identity expert",
+                   "T": T, "H": H, "E": E, "k": k, "R": R, "nodes": N, "max_tokens": M,
+                   "pairs": pairs, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between steps (256 MiB write outside the timed events)"},
+        "tokens_per_s": round(world * T / (ms * 1e-3), 1),
+        "frac_of_hbm_peak": round(value / world / peak, 4),
+        "stages": stages,
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "alg_bytes_per_launch": b[dom], "traffic_note": traffic_note},
+        "e2e": {"value": round(world * total_bytes / (e2e_t * 1e-3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_t, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+        "extra_workloads": extra,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    return line
+
+
+def time_events(fn, n, flush, stream):
+    ms = []
+    for _ in range(n):
+        flush.zero_()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        z.record(stream)
+        ms.append((a, z))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(z) for a, z in ms)
+
+
+def extra_stages(ep, dev, args, flush, peak):
+    """Per-stage device times of the other workloads (FP8 dispatch, restripe + node dispatch,
+    skewed routing). Each is timed with CUDA events, L2 flushed before every launch."""
+    stream = torch.cuda.current_stream()
+    n = max(3, min(args.steps, 10))
+    res = {}
+
+    def gbs(bytes_, ms):
+        return {"ms": round(ms, 4), "alg_bytes": bytes_, "gbs": round(bytes_ / (ms * 1e-3) / 1e9, 1),
+                "frac_of_hbm_peak": round(bytes_ / (ms * 1e-3) / 1e9 / peak, 4)}
+
+    # FP8 dispatch (dsv3 shape)
+    w = workloads.make("dsv3_fp8")
+    x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(w.topk_idx).to(dev)
+    tw = torch.from_numpy(w.topk_w).to(dev)
+    lay = ep.get_layout(topk, w.E, w.R, w.ranks_per_node)
+    d = ep.alloc_dispatch(w.R, w.max_tokens, w.H, w.k, fp8=True, device=dev)
+    ep.dispatch(x, topk, tw, lay, w.max_tokens, fp8=True, out=d)
+    pairs = int(lay.tokens_per_rank.sum().item())
+    ms = time_events(lambda: ep.dispatch(x, topk, tw, lay, w.max_tokens, fp8=True, out=d), n, flush, stream)
+    row = w.H + 4 * (w.H // 128)
+    b = step_bytes(w.T, w.H, w.k, w.E, w.R, w.num_nodes, pairs, row_bytes_out=row)["dispatch"]
+    res["dsv3_fp8_dispatch"] = gbs(b, ms)
+    del d, x, lay
+
+    # restripe + node dispatch (T=8192, H=7168, 8 nodes, P=128)
+    w = workloads.make("restripe")
+    x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(w.topk_idx).to(dev)
+    lay = ep.get_layout(topk, w.E, w.R, w.ranks_per_node)
+    prob = torch.from_numpy(w.prob).to(dev)
+    Nn, T, M, P, H = w.num_nodes, w.T, w.max_tokens, w.prob.shape[2], w.H
+    staging = torch.empty((Nn, M, P), dtype=torch.float32, device=dev)
+    ms = time_events(lambda: ep.ep_restripe_prob(prob, M, staging), n, flush, stream)
+    res["restripe_prob"] = gbs(2 * T * Nn * P * 4, ms)
+    rx = torch.empty((Nn, M, H), dtype=torch.bfloat16, device=dev)
+    rp = torch.empty((Nn, M, P), dtype=torch.float32, device=dev)
+    routed = int(lay.is_token_in_node.sum().item())
+    for name, mode, dests in (("node_dispatch_sparse", ep.NODES_SPARSE, routed),
+                              ("node_dispatch_dense", ep.NODES_DENSE, Nn * T)):
+        fn = lambda mode=mode: ep.ep_dispatch_nodes(x, staging, lay.is_token_in_node, Nn, M, w.chunk_tokens, mode,
+                                                    rx, rp)
+        fn()
+        ms = time_events(fn, n, flush, stream)
+        res[name] = gbs(T * 2 * H + dests * (2 * H + 2 * P * 4) + (T * Nn if mode == ep.NODES_SPARSE else 0), ms)
+    del rx, rp, staging, prob, x, lay
+
+    # skewed routing dispatch + combine (T=16384, H=4096, R=64, max_tokens = hottest rank)
+    w = workloads.make("skewed")
+    x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(w.topk_idx).to(dev)
+    tw = torch.from_numpy(w.topk_w).to(dev)
+    lay = ep.get_layout(topk, w.E, w.R, w.ranks_per_node)
+    M = int(lay.tokens_per_rank.max().item())
+    pairs = int(lay.tokens_per_rank.sum().item())
+    d = ep.alloc_dispatch(w.R, M, w.H, w.k, device=dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    ms_l = time_events(lambda: ep.get_layout(topk, w.E, w.R, w.ranks_per_node, out=lay), n, flush, stream)
+    ep.dispatch(x, topk, tw, lay, M, out=d)
+    ms_d = time_events(lambda: ep.dispatch(x, topk, tw, lay, M, out=d), n, flush, stream)
+    ms_c = time_events(lambda: ep.combine(d.recv_x, lay, M, out=out), n, flush, stream)
+    b = step_bytes(w.T, w.H, w.k, w.E, w.R, w.num_nodes, pairs)
+    res["skewed_layout"] = gbs(b["layout"], ms_l)
+    res["skewed_dispatch"] = gbs(b["dispatch"], ms_d)
+    res["skewed_combine"] = gbs(b["combine"], ms_c)
+    res["skewed_hottest_rank_tokens"] = M
+    res["skewed_mean_rank_tokens"] = round(pairs / w.R, 1)
+    return res
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    """The oracle (plain single-threaded C) on the host cores, same metric and workload."""
+    import oracle
+
+    oracle.build()
+    w = workloads.make("dsv3")
+    tokens = w.T
+    for _ in range(args.warmup):
+        oracle_step_seconds(w, tokens, tokens)
+    times = []
+    pairs = 0
+    for _ in range(args.steps):
+        dt, pairs = oracle_step_seconds(w, tokens, tokens)
+        times.append(dt)
+    s = statistics.mean(times)
+    b = step_bytes(tokens, w.H, w.k, w.E, w.R, w.num_nodes, pairs)
+    value = sum(b.values()) / s / 1e9
+    sample = (f"each step: the oracle's layout+dispatch+identity combine on all {tokens} tokens of the "
+              f"dsv3 workload, single-threaded C on one host core")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(s * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "dsv3 prefill: T=4096 H=7168 bf16, E=256 top-8, R=32 virtual ranks "
+                               "(8 nodes x 4), max_tokens=4096, identity expert"},
+        "tokens_per_s": round(tokens / s, 1),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--skip-extra", action="store_true", help="skip the other workloads' stage timings")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        log("warmup raised to 3 (minimum)")
+        args.warmup = 3
+    if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; other ranks have no work
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        print(json.dumps(run_reference(args, world, 0)), flush=True)
+        return 0
+    world, rank, _ = dist_setup()
+    line = run_ours(args, world, rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,24 @@
+"""GB300 (sm_103a) expert-parallel dispatch / combine.
+
+The single-GPU data-parallel hot path of MoE expert-parallel dispatch and
+combine, with R virtual EP ranks held as slabs of one GPU's HBM:
+
+  ep_get_layout      counts, is_token_in_rank / node, stable slots (one kernel)
+  ep_dispatch        destination-major permute of bf16 rows or fused 1x128 E4M3
+  ep_restripe_prob   prob [T][nodes][P] -> [nodes][max_tokens][P]
+  ep_dispatch_nodes  node-level dense / sparse (run-length) dispatch
+  ep_combine         fp32 ascending-rank gather-reduce back to token order
+
+The C ABI is include/ep.h (libep_gb300.so, built in-tree by build.py); the
+functions here with the same names are its ctypes binding, and api.py
+allocates buffers and chains the calls.
+"""
+from ._lib import (  # noqa: F401
+    ABI_VERSION, DTYPE_BF16, DTYPE_E4M3, EP_ERR_CUDA, EP_ERR_INVALID, EP_OK, EXPORTS, FLAG_BAD_EXPERT,
+    FLAG_CAPACITY, FLAG_TIMEOUT, FLAG_WORKSPACE, NODES_DENSE, NODES_SPARSE, EpError, ep_combine, ep_dispatch,
+    ep_dispatch_nodes, ep_get_layout, ep_layout_workspace_size, ep_restripe_prob, lib,
+)
+from .api import (  # noqa: F401
+    Dispatched, Layout, alloc_dispatch, alloc_layout, combine, dispatch, get_layout, read_flags,
+)
+from .build import LIB_PATH, build as build_library  # noqa: F401

@@ -1,0 +1,100 @@
+// ep_combine.cu -- combine: gather every rank's expert output for a token and
+// reduce it back in token order ("[PR #347] Feature/sm free normal kernel",
+// 2.1 Feature; BF16 combine of 3.2.1).
+//
+//   out[t][h] = bf16_rn( ((0 + y[r0][s0][h]) + y[r1][s1][h]) + ... ),  r0 < r1 < ...
+//
+// One warp per token: the warp reads the token's slot row once (lanes across
+// ranks), compacts the contributing rows in ascending rank order with a ballot,
+// then for each 16-byte vector of the output (8 channels per lane) issues the
+// loads of up to 8 source rows at once and adds them into fp32 accumulators
+// strictly in that order (one IEEE addition per term, no reassociation), and
+// stores one bf16 vector rounded to nearest even. The kernel is bound by HBM
+// bandwidth: it reads one row per (token, rank) pair and writes T rows.
+#include "ep_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxSrc = 256;  // = largest R: every rank may contribute
+constexpr int kBatch = 8;  // source rows loaded together
+
+__device__ __forceinline__ void add8(float* acc, const uint4& v) {
+    acc[0] = __fadd_rn(acc[0], ep::bf16_lo(v.x));
+    acc[1] = __fadd_rn(acc[1], ep::bf16_hi(v.x));
+    acc[2] = __fadd_rn(acc[2], ep::bf16_lo(v.y));
+    acc[3] = __fadd_rn(acc[3], ep::bf16_hi(v.y));
+    acc[4] = __fadd_rn(acc[4], ep::bf16_lo(v.z));
+    acc[5] = __fadd_rn(acc[5], ep::bf16_hi(v.z));
+    acc[6] = __fadd_rn(acc[6], ep::bf16_lo(v.w));
+    acc[7] = __fadd_rn(acc[7], ep::bf16_hi(v.w));
+}
+
+__global__ void __launch_bounds__(kThreads)
+    combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ slot, int T, int H, int R,
+                   int max_tokens, uint16_t* __restrict__ out, int32_t* status) {
+    __shared__ long long s_src[kWarps][kMaxSrc];
+    const int lane = ep::lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int nvec = H / 8;
+    const uint4* ys = reinterpret_cast<const uint4*>(y);
+    uint4* os = reinterpret_cast<uint4*>(out);
+
+    for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
+        int ns = 0;
+        bool over_any = false;
+        for (int r0 = 0; r0 < R; r0 += 32) {
+            const int r = r0 + lane;
+            const int s = r < R ? slot[static_cast<size_t>(t) * R + r] : -1;
+            const bool over = s >= max_tokens;
+            over_any |= over;
+            const bool ok = s >= 0 && !over;
+            const uint32_t m = __ballot_sync(ep::kFullMask, ok);
+            if (ok) {
+                const int pos = ns + __popc(m & ep::lanemask_lt());
+                s_src[warp][pos] = (static_cast<long long>(r) * max_tokens + s) * nvec;
+            }
+            ns += __popc(m);
+        }
+        if (over_any) ep::raise_flag(status, EP_FLAG_CAPACITY);
+        __syncwarp();
+
+        for (int v = lane; v < nvec; v += 32) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int d0 = 0; d0 < ns; d0 += kBatch) {
+                uint4 buf[kBatch];
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i)
+                    if (d0 + i < ns) buf[i] = ep::ld_stream_v4(ys + s_src[warp][d0 + i] + v);
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i)
+                    if (d0 + i < ns) add8(acc, buf[i]);
+            }
+            uint4 o;
+            o.x = ep::pack_bf16x2_rn(acc[0], acc[1]);
+            o.y = ep::pack_bf16x2_rn(acc[2], acc[3]);
+            o.z = ep::pack_bf16x2_rn(acc[4], acc[5]);
+            o.w = ep::pack_bf16x2_rn(acc[6], acc[7]);
+            ep::st_v4(os + static_cast<size_t>(t) * nvec + v, o);
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+extern "C" ep_status_t ep_combine(const void* y, const int32_t* slot, int32_t T, int32_t H, int32_t R,
+                                  int32_t max_tokens, void* out, int32_t* status, void* stream) {
+    using namespace ep;
+    if (T < 0 || H <= 0 || H % 8 != 0 || R < 1 || R > 256 || max_tokens < 0) return EP_ERR_INVALID;
+    if (T == 0) return EP_OK;
+    if (slot == nullptr || out == nullptr || (max_tokens > 0 && y == nullptr)) return EP_ERR_INVALID;
+    if (!aligned16_or_null(y) || !aligned16(slot) || !aligned16(out)) return EP_ERR_INVALID;
+    const int want = (T + kWarps - 1) / kWarps;
+    const int cap = sm_count() * 8;
+    const int grid = want < cap ? want : cap;
+    combine_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(static_cast<const uint16_t*>(y), slot, T, H, R,
+                                                             max_tokens, static_cast<uint16_t*>(out), status);
+    return check_launch();
+}

@@ -1,0 +1,247 @@
+// ep_dispatch.cu -- rank-level dispatch: every token goes once to every rank it
+// routes to, into that rank's slab of the destination-major receive buffers
+// ("[PR #347] Feature/sm free normal kernel", 2.1 Feature; workload of 3.1;
+// FP8 and BF16 dispatch of 3.2.1), with the optional per-token 1x128 E4M3
+// quantisation fused into the copy.
+//
+// Design: a persistent grid of warps, one token per warp at a time. The warp
+// reads the token's slot row once (lanes across ranks) and compacts the
+// destinations (ascending rank) into shared memory with a ballot; then it
+// streams the hidden row through registers in 16-byte vectors, reading each
+// vector once from HBM and storing it to every destination slab. Metadata
+// (source index, local expert ids, weights) is written by one lane per
+// destination. Nothing here is a contraction, so no tensor cores: the kernel
+// is bound by HBM bandwidth (read T rows, write one row per (token, rank)).
+#include "ep_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxDest = 256;  // = largest R: a slot row may name every rank
+constexpr int kMaxTopk = 32;
+constexpr int kUnroll = 4;     // 16-byte vectors in flight per lane (bf16 path)
+constexpr int kUnrollFp8 = 2;  // warp iterations (2 blocks of 128 each) in flight (FP8 path)
+
+struct DispatchArgs {
+    const uint16_t* x;
+    const int64_t* topk_idx;
+    const float* topk_w;
+    const int32_t* slot;
+    int T, H, k, E, R, epr, max_tokens;
+    void* recv_x;
+    float* recv_scales;
+    int32_t* recv_src_idx;
+    int32_t* recv_topk_idx;
+    float* recv_topk_w;
+    int32_t* status;
+};
+
+// Destinations of token t: compacted (ascending rank) into s_rank / s_row.
+// Returns their number; drops slots >= max_tokens (EP_FLAG_CAPACITY).
+__device__ __forceinline__ int gather_destinations(const DispatchArgs& a, int t, int* s_rank, long long* s_row) {
+    const int lane = ep::lane_id();
+    int nd = 0;
+    bool over_any = false;
+    for (int r0 = 0; r0 < a.R; r0 += 32) {
+        const int r = r0 + lane;
+        const int s = r < a.R ? a.slot[static_cast<size_t>(t) * a.R + r] : -1;
+        const bool over = s >= a.max_tokens;
+        over_any |= over;
+        const bool ok = s >= 0 && !over;
+        const uint32_t m = __ballot_sync(ep::kFullMask, ok);
+        if (ok) {
+            const int pos = nd + __popc(m & ep::lanemask_lt());
+            s_rank[pos] = r;
+            s_row[pos] = static_cast<long long>(r) * a.max_tokens + s;
+        }
+        nd += __popc(m);
+    }
+    if (over_any) ep::raise_flag(a.status, EP_FLAG_CAPACITY);
+    __syncwarp();
+    return nd;
+}
+
+__device__ __forceinline__ void write_metadata(const DispatchArgs& a, int t, int nd, const int* s_rank,
+                                               const long long* s_row) {
+    const int lane = ep::lane_id();
+    if (lane == 0) {
+        bool bad = false;
+        for (int j = 0; j < a.k; ++j) bad |= a.topk_idx[static_cast<size_t>(t) * a.k + j] >= a.E;
+        if (bad) ep::raise_flag(a.status, EP_FLAG_BAD_EXPERT);
+    }
+    const int64_t* ids = a.topk_idx + static_cast<size_t>(t) * a.k;
+    for (int d = lane; d < nd; d += 32) {
+        const int r = s_rank[d];
+        const size_t row = static_cast<size_t>(s_row[d]);
+        if (a.recv_src_idx != nullptr) a.recv_src_idx[row] = t;
+        for (int j = 0; j < a.k; ++j) {
+            const int64_t e = ids[j];
+            const bool on = e >= 0 && e < a.E && static_cast<int>(e) / a.epr == r;
+            if (a.recv_topk_idx != nullptr)
+                a.recv_topk_idx[row * a.k + j] = on ? static_cast<int32_t>(e) - r * a.epr : -1;
+            if (a.recv_topk_w != nullptr)
+                a.recv_topk_w[row * a.k + j] = on ? a.topk_w[static_cast<size_t>(t) * a.k + j] : 0.0f;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(DispatchArgs a) {
+    __shared__ int s_rank[kWarps][kMaxDest];
+    __shared__ long long s_row[kWarps][kMaxDest];
+    const int lane = ep::lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int nvec = a.H / 8;  // 16-byte vectors per row
+    uint4* recv = static_cast<uint4*>(a.recv_x);
+
+    for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
+        const int nd = gather_destinations(a, t, s_rank[warp], s_row[warp]);
+        write_metadata(a, t, nd, s_rank[warp], s_row[warp]);
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H);
+        for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
+            uint4 buf[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nvec) buf[u] = ep::ld_stream_v4(src + v);
+            }
+            for (int d = 0; d < nd; ++d) {
+                uint4* dst = recv + static_cast<size_t>(s_row[warp][d]) * nvec;
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int v = v0 + u * 32 + lane;
+                    if (v < nvec) ep::st_v4(dst + v, buf[u]);
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// One 128-element block held by a half warp: 8 bf16 per lane.
+// Returns the 8 E4M3 codes (lo word: elements 0..3, hi word: 4..7) and the scale.
+__device__ __forceinline__ void quantize8(const uint4& v, uint32_t& q_lo, uint32_t& q_hi, float& scale) {
+    float f[8];
+    f[0] = ep::bf16_lo(v.x); f[1] = ep::bf16_hi(v.x);
+    f[2] = ep::bf16_lo(v.y); f[3] = ep::bf16_hi(v.y);
+    f[4] = ep::bf16_lo(v.z); f[5] = ep::bf16_hi(v.z);
+    f[6] = ep::bf16_lo(v.w); f[7] = ep::bf16_hi(v.w);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    // max over the 16 lanes of this half warp (xor offsets < 16 stay in the half)
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(ep::kFullMask, amax, off));
+    scale = __fdiv_rn(amax, 448.0f);
+    uint32_t c[4];
+    if (amax == 0.0f) {
+        // all elements are +-0: keep the sign of each zero
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            c[i] = ((__float_as_uint(f[2 * i]) >> 31) ? 0x80u : 0u) |
+                   ((__float_as_uint(f[2 * i + 1]) >> 31) ? 0x8000u : 0u);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            c[i] = ep::pack_e4m3x2_rn_sat(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+    }
+    q_lo = c[0] | (c[1] << 16);
+    q_hi = c[2] | (c[3] << 16);
+}
+
+__global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a) {
+    __shared__ int s_rank[kWarps][kMaxDest];
+    __shared__ long long s_row[kWarps][kMaxDest];
+    const int lane = ep::lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int nblk = a.H / 128;
+    const int half = lane >> 4;   // which of the two blocks of a warp iteration
+    const int hl = lane & 15;     // 16-byte vector within the block
+    uint8_t* recv = static_cast<uint8_t*>(a.recv_x);
+
+    for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
+        const int nd = gather_destinations(a, t, s_rank[warp], s_row[warp]);
+        write_metadata(a, t, nd, s_rank[warp], s_row[warp]);
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H);
+        for (int b0 = 0; b0 < nblk; b0 += 2 * kUnrollFp8) {
+            uint4 in[kUnrollFp8];
+#pragma unroll
+            for (int u = 0; u < kUnrollFp8; ++u) {
+                const int b = b0 + 2 * u + half;
+                in[u] = b < nblk ? ep::ld_stream_v4(src + b * 16 + hl) : make_uint4(0, 0, 0, 0);
+            }
+            uint32_t qlo[kUnrollFp8], qhi[kUnrollFp8];
+            float sc[kUnrollFp8];
+#pragma unroll
+            for (int u = 0; u < kUnrollFp8; ++u) quantize8(in[u], qlo[u], qhi[u], sc[u]);
+            for (int d = 0; d < nd; ++d) {
+                const size_t row = static_cast<size_t>(s_row[warp][d]);
+                uint8_t* dst = recv + row * a.H;
+                float* dsc = a.recv_scales + row * nblk;
+#pragma unroll
+                for (int u = 0; u < kUnrollFp8; ++u) {
+                    const int b = b0 + 2 * u + half;
+                    if (b < nblk) {
+                        ep::st_v2(dst + b * 128 + hl * 8, qlo[u], qhi[u]);
+                        if (hl == 0) dsc[b] = sc[u];
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+int grid_for(int T, int blocks_per_sm) {
+    const int want = (T + kWarps - 1) / kWarps;
+    const int cap = ep::sm_count() * blocks_per_sm;
+    return want < 1 ? 1 : (want < cap ? want : cap);
+}
+
+}  // namespace
+
+extern "C" ep_status_t ep_dispatch(const void* x, ep_dtype_t out_dtype, const int64_t* topk_idx,
+                                   const float* topk_w, const int32_t* slot, int32_t T, int32_t H, int32_t k,
+                                   int32_t E, int32_t R, int32_t max_tokens, void* recv_x, float* recv_scales,
+                                   int32_t* recv_src_idx, int32_t* recv_topk_idx, float* recv_topk_w,
+                                   int32_t* status, void* stream) {
+    using namespace ep;
+    const bool fp8 = out_dtype == EP_DTYPE_E4M3;
+    if (out_dtype != EP_DTYPE_BF16 && !fp8) return EP_ERR_INVALID;
+    if (T < 0 || H <= 0 || H % 8 != 0 || (fp8 && H % 128 != 0) || k < 1 || k > kMaxTopk || R < 1 ||
+        R > 256 || E < R || E % R != 0 || max_tokens < 0)
+        return EP_ERR_INVALID;
+    if (recv_x == nullptr || (fp8 && recv_scales == nullptr) || (!fp8 && recv_scales != nullptr))
+        return EP_ERR_INVALID;
+    if (T > 0 && (x == nullptr || topk_idx == nullptr || slot == nullptr)) return EP_ERR_INVALID;
+    if (recv_topk_w != nullptr && T > 0 && topk_w == nullptr) return EP_ERR_INVALID;
+    if (!aligned16_or_null(x) || !aligned16_or_null(topk_idx) || !aligned16_or_null(topk_w) ||
+        !aligned16_or_null(slot) || !aligned16(recv_x) || !aligned16_or_null(recv_scales) ||
+        !aligned16_or_null(recv_src_idx) || !aligned16_or_null(recv_topk_idx) || !aligned16_or_null(recv_topk_w))
+        return EP_ERR_INVALID;
+    if (T == 0) return EP_OK;
+    DispatchArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.slot = slot;
+    a.T = T;
+    a.H = H;
+    a.k = k;
+    a.E = E;
+    a.R = R;
+    a.epr = E / R;
+    a.max_tokens = max_tokens;
+    a.recv_x = recv_x;
+    a.recv_scales = recv_scales;
+    a.recv_src_idx = recv_src_idx;
+    a.recv_topk_idx = recv_topk_idx;
+    a.recv_topk_w = recv_topk_w;
+    a.status = status;
+    const int grid = grid_for(T, 8);
+    if (fp8)
+        dispatch_fp8_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(a);
+    else
+        dispatch_bf16_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(a);
+    return check_launch();
+}

@@ -1,0 +1,317 @@
+// ep_layout.cu -- routing layout: per-expert / per-rank / per-node counts,
+// is_token_in_rank / is_token_in_node and the stable slot of every (token, rank).
+//
+// The layout step is DeepEP's get_dispatch_layout ("[PR #347] Feature/sm free
+// normal kernel", commit "add arg return_recv_hook for get_dispatch_layout");
+// the slots are the scan of "[PR #634] Hybrid ep nixl restripe" (commit "fix
+// scan permute-fusion local-experts sum array sizing"): slot[t][r] is the
+// number of earlier tokens that also go to rank r.
+//
+// One launch, one tile of 256 tokens per CTA (thread = token):
+//   1. each thread reads its token's k expert ids, bumps a shared-memory expert
+//      histogram and forms its rank bit mask (R <= 256: four 64-bit words);
+//   2. per rank, one warp ballot gives the 32-token membership mask of each
+//      warp; popcounts give per-warp counts and in-warp prefixes;
+//   3. the tile's per-rank counts are scanned across tiles with a decoupled
+//      look-back: every (tile, rank) publishes one 64-bit word holding
+//      {epoch, state, count}; state 1 = this tile's count only, state 2 = the
+//      inclusive prefix. Tiles are numbered by an atomic ticket, so a tile waits
+//      only on tiles whose CTAs already run; every wait is bounded in time and
+//      raises EP_FLAG_TIMEOUT when it gives up;
+//   4. the tile writes is_token_in_rank / slot / is_token_in_node rows with
+//      lanes across ranks (coalesced);
+//   5. expert and node counts are accumulated with atomics in the workspace;
+//      the last CTA to finish moves them to the outputs, zeroes the
+//      accumulators and the counters and advances the epoch, so the workspace
+//      is ready for the next call without a memset.
+#include "ep_common.cuh"
+
+namespace {
+
+using namespace ep;
+
+constexpr int kTileTokens = 256;  // = threads per CTA
+constexpr int kTileWarps = kTileTokens / 32;
+constexpr int kMaxRanks = 256;
+constexpr int kMaxExperts = 8192;
+constexpr int kMaxTopk = 32;
+constexpr uint32_t kStateAggregate = 1u;
+constexpr uint32_t kStatePrefix = 2u;
+constexpr int kLookbackBatch = 8;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
+constexpr uint32_t kWaitLimitIters = 1u << 24;               // hard cap on polls
+
+struct LayoutArgs {
+    const int64_t* topk_idx;
+    int T, k, E, R, rpn, N, epr, num_tiles;
+    int32_t* tokens_per_expert;
+    int32_t* tokens_per_rank;
+    int32_t* tokens_per_node;
+    uint8_t* in_rank;
+    uint8_t* in_node;
+    int32_t* slot;
+    ep_layout_ws_header_t* hdr;
+    unsigned long long* words;  // [num_tiles][R]
+    int32_t* acc_expert;        // [E]
+    int32_t* acc_node;          // [N]
+    int32_t* status;
+};
+
+__host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+inline int num_tiles_for(int T) { return T > 0 ? (T + kTileTokens - 1) / kTileTokens : 1; }
+
+__device__ __forceinline__ unsigned long long pack_word(uint32_t epoch, uint32_t state, uint32_t v) {
+    return (static_cast<unsigned long long>(epoch) << 32) | (static_cast<unsigned long long>(state) << 30) |
+           static_cast<unsigned long long>(v & 0x3fffffffu);
+}
+__device__ __forceinline__ uint32_t word_epoch(unsigned long long w) { return static_cast<uint32_t>(w >> 32); }
+__device__ __forceinline__ uint32_t word_state(unsigned long long w) { return static_cast<uint32_t>(w >> 30) & 3u; }
+__device__ __forceinline__ uint32_t word_value(unsigned long long w) { return static_cast<uint32_t>(w) & 0x3fffffffu; }
+
+__device__ __forceinline__ uint64_t pick_word(uint64_t m0, uint64_t m1, uint64_t m2, uint64_t m3, int r) {
+    return r < 64 ? m0 : (r < 128 ? m1 : (r < 192 ? m2 : m3));
+}
+
+__global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
+    extern __shared__ int32_t s_hist[];  // [E]
+    __shared__ uint32_t s_mask[kTileWarps][kMaxRanks];
+    __shared__ int32_t s_wpref[kTileWarps][kMaxRanks];
+    __shared__ int32_t s_tile_prefix[kMaxRanks];
+    __shared__ uint32_t s_tile, s_epoch, s_stall, s_last;
+
+    const int tid = static_cast<int>(threadIdx.x);
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+
+    if (tid == 0) {
+        s_tile = atomicAdd(&a.hdr->ticket, 1u);
+        s_epoch = ld_relaxed_u32(&a.hdr->epoch) + 1u;
+        s_stall = ld_relaxed_u32(&a.hdr->stall_tile);
+    }
+    for (int e = tid; e < a.E; e += kTileTokens) s_hist[e] = 0;
+    __syncthreads();
+
+    if (s_tile >= static_cast<uint32_t>(a.num_tiles)) {
+        // the workspace was not at rest (not zero-filled, or shared by concurrent
+        // calls): touch nothing, report it; the caller zero-fills it again
+        if (tid == 0) raise_flag(a.status, EP_FLAG_WORKSPACE);
+        return;
+    }
+    const int tile = static_cast<int>(s_tile);
+    const uint32_t epoch = s_epoch;
+    const bool stalled = s_stall == static_cast<uint32_t>(tile) + 1u;
+    const int t0 = tile * kTileTokens;
+    const int t = t0 + tid;
+
+    // 1. token -> rank mask, expert histogram
+    uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
+    if (t < a.T) {
+        const int64_t* row = a.topk_idx + static_cast<size_t>(t) * a.k;
+        bool bad = false;
+        for (int j = 0; j < a.k; ++j) {
+            const int64_t e = row[j];
+            if (e < 0) continue;
+            if (e >= a.E) {
+                bad = true;
+                continue;
+            }
+            atomicAdd(&s_hist[e], 1);
+            const int r = static_cast<int>(e) / a.epr;
+            const uint64_t bit = 1ull << (r & 63);
+            if (r < 64) m0 |= bit;
+            else if (r < 128) m1 |= bit;
+            else if (r < 192) m2 |= bit;
+            else m3 |= bit;
+        }
+        if (bad) raise_flag(a.status, EP_FLAG_BAD_EXPERT);
+    }
+
+    // 2. per-rank warp membership masks
+    for (int r = 0; r < a.R; ++r) {
+        const uint32_t bit = static_cast<uint32_t>(pick_word(m0, m1, m2, m3, r) >> (r & 63)) & 1u;
+        const uint32_t m = __ballot_sync(kFullMask, bit);
+        if (lane == (r & 31)) s_mask[warp][r] = m;
+    }
+    __syncthreads();
+
+    // expert and node counts of this tile -> workspace accumulators
+    for (int e = tid; e < a.E; e += kTileTokens) {
+        const int c = s_hist[e];
+        if (c != 0) atomicAdd(&a.acc_expert[e], c);
+    }
+    for (int n = tid; n < a.N; n += kTileTokens) {
+        int c = 0;
+        for (int w = 0; w < kTileWarps; ++w) {
+            uint32_t m = 0;
+            for (int q = 0; q < a.rpn; ++q) m |= s_mask[w][n * a.rpn + q];
+            c += __popc(m);
+        }
+        if (c != 0) atomicAdd(&a.acc_node[n], c);
+    }
+
+    // 3. per-rank scan across tiles (decoupled look-back), thread r owns rank r
+    if (tid < a.R) {
+        const int r = tid;
+        int run = 0;
+        for (int w = 0; w < kTileWarps; ++w) {
+            s_wpref[w][r] = run;
+            run += __popc(s_mask[w][r]);
+        }
+        const uint32_t agg = static_cast<uint32_t>(run);
+        unsigned long long* my_word = a.words + static_cast<size_t>(tile) * a.R + r;
+        if (!stalled) st_relaxed_u64(my_word, pack_word(epoch, tile == 0 ? kStatePrefix : kStateAggregate, agg));
+
+        uint32_t excl = 0;
+        bool timed_out = false;
+        int j = tile - 1;
+        while (j >= 0 && !timed_out) {
+            const int nb = j + 1 < kLookbackBatch ? j + 1 : kLookbackBatch;
+            unsigned long long wv[kLookbackBatch];
+#pragma unroll
+            for (int i = 0; i < kLookbackBatch; ++i)
+                if (i < nb) wv[i] = ld_relaxed_u64(a.words + static_cast<size_t>(j - i) * a.R + r);
+            bool found_prefix = false;
+#pragma unroll
+            for (int i = 0; i < kLookbackBatch; ++i) {
+                if (i >= nb || found_prefix || timed_out) continue;
+                const unsigned long long* p = a.words + static_cast<size_t>(j - i) * a.R + r;
+                unsigned long long w = wv[i];
+                if (word_epoch(w) != epoch || word_state(w) == 0u) {
+                    const unsigned long long start = globaltimer_ns();
+                    uint32_t polls = 0;
+                    while (word_epoch(w) != epoch || word_state(w) == 0u) {
+                        if (++polls >= kWaitLimitIters || globaltimer_ns() - start > kWaitLimitNs) {
+                            timed_out = true;
+                            break;
+                        }
+                        if (polls > 16) __nanosleep(256);
+                        w = ld_relaxed_u64(p);
+                    }
+                    if (timed_out) break;
+                }
+                excl += word_value(w);
+                if (word_state(w) == kStatePrefix) found_prefix = true;
+            }
+            if (found_prefix) break;
+            j -= nb;
+        }
+        if (timed_out) raise_flag(a.status, EP_FLAG_TIMEOUT);
+        if (tile > 0 && !stalled) st_relaxed_u64(my_word, pack_word(epoch, kStatePrefix, excl + agg));
+        s_tile_prefix[r] = static_cast<int32_t>(excl);
+        if (tile == a.num_tiles - 1) a.tokens_per_rank[r] = static_cast<int32_t>(excl + agg);
+    }
+    __syncthreads();
+
+    // 4. rows of is_token_in_rank / slot / is_token_in_node, lanes across ranks
+    const int ntok = a.T - t0 < kTileTokens ? a.T - t0 : kTileTokens;
+    for (int tl = warp; tl < ntok; tl += kTileWarps) {
+        const int w = tl >> 5;
+        const int ln = tl & 31;
+        const uint32_t below = (1u << ln) - 1u;
+        const size_t base = static_cast<size_t>(t0 + tl) * a.R;
+        for (int r = lane; r < a.R; r += 32) {
+            const uint32_t m = s_mask[w][r];
+            const bool in = (m >> ln) & 1u;
+            a.in_rank[base + r] = in ? 1 : 0;
+            a.slot[base + r] = in ? s_tile_prefix[r] + s_wpref[w][r] + __popc(m & below) : -1;
+        }
+        if (a.in_node != nullptr) {
+            const size_t nbase = static_cast<size_t>(t0 + tl) * a.N;
+            for (int n = lane; n < a.N; n += 32) {
+                uint32_t m = 0;
+                for (int q = 0; q < a.rpn; ++q) m |= s_mask[w][n * a.rpn + q];
+                a.in_node[nbase + n] = (m >> ln) & 1u;
+            }
+        }
+    }
+
+    // 5. last CTA: move the accumulated counts out and reset the workspace
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&a.hdr->done, 1u) == static_cast<uint32_t>(a.num_tiles - 1);
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (int e = tid; e < a.E; e += kTileTokens) a.tokens_per_expert[e] = atomicExch(&a.acc_expert[e], 0);
+        for (int n = tid; n < a.N; n += kTileTokens) a.tokens_per_node[n] = atomicExch(&a.acc_node[n], 0);
+        if (tid == 0) {
+            atomicExch(&a.hdr->ticket, 0u);
+            atomicExch(&a.hdr->done, 0u);
+            atomicExch(&a.hdr->epoch, epoch);
+        }
+    }
+}
+
+bool g_smem_attr_set[64] = {};
+
+}  // namespace
+
+extern "C" size_t ep_layout_workspace_size(int32_t T, int32_t E, int32_t R, int32_t ranks_per_node) {
+    if (T < 0 || E <= 0 || R <= 0) return 0;
+    const int N = ranks_per_node > 0 ? R / ranks_per_node : 0;
+    return align256(sizeof(ep_layout_ws_header_t)) +
+           align256(static_cast<size_t>(num_tiles_for(T)) * R * sizeof(unsigned long long)) +
+           align256(static_cast<size_t>(E) * sizeof(int32_t)) + align256(static_cast<size_t>(N) * sizeof(int32_t));
+}
+
+extern "C" ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E, int32_t R,
+                                     int32_t ranks_per_node, int32_t* tokens_per_expert,
+                                     int32_t* tokens_per_rank, int32_t* tokens_per_node,
+                                     uint8_t* is_token_in_rank, uint8_t* is_token_in_node, int32_t* slot,
+                                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+    using namespace ep;
+    if (T < 0 || T >= (1 << 30) || k < 1 || k > kMaxTopk || R < 1 || R > kMaxRanks || E < R ||
+        E > kMaxExperts || E % R != 0 || ranks_per_node < 0 || ranks_per_node > R ||
+        (ranks_per_node > 0 && R % ranks_per_node != 0))
+        return EP_ERR_INVALID;
+    const bool nodes = ranks_per_node > 0;
+    if (tokens_per_expert == nullptr || tokens_per_rank == nullptr || workspace == nullptr)
+        return EP_ERR_INVALID;
+    if (T > 0 && (topk_idx == nullptr || is_token_in_rank == nullptr || slot == nullptr)) return EP_ERR_INVALID;
+    if (nodes && (tokens_per_node == nullptr || (T > 0 && is_token_in_node == nullptr))) return EP_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EP_ERR_INVALID;
+    if (workspace_bytes < ep_layout_workspace_size(T, E, R, ranks_per_node)) return EP_ERR_INVALID;
+    if (!aligned16_or_null(topk_idx) || !aligned16(tokens_per_expert) || !aligned16(tokens_per_rank) ||
+        !aligned16_or_null(tokens_per_node) || !aligned16_or_null(is_token_in_rank) ||
+        !aligned16_or_null(is_token_in_node) || !aligned16_or_null(slot))
+        return EP_ERR_INVALID;
+
+    LayoutArgs a{};
+    a.topk_idx = topk_idx;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.R = R;
+    a.rpn = nodes ? ranks_per_node : 1;
+    a.N = nodes ? R / ranks_per_node : 0;
+    a.epr = E / R;
+    a.num_tiles = num_tiles_for(T);
+    a.tokens_per_expert = tokens_per_expert;
+    a.tokens_per_rank = tokens_per_rank;
+    a.tokens_per_node = nodes ? tokens_per_node : nullptr;
+    a.in_rank = is_token_in_rank;
+    a.in_node = nodes ? is_token_in_node : nullptr;
+    a.slot = slot;
+    char* ws = static_cast<char*>(workspace);
+    a.hdr = reinterpret_cast<ep_layout_ws_header_t*>(ws);
+    ws += align256(sizeof(ep_layout_ws_header_t));
+    a.words = reinterpret_cast<unsigned long long*>(ws);
+    ws += align256(static_cast<size_t>(a.num_tiles) * R * sizeof(unsigned long long));
+    a.acc_expert = reinterpret_cast<int32_t*>(ws);
+    ws += align256(static_cast<size_t>(E) * sizeof(int32_t));
+    a.acc_node = reinterpret_cast<int32_t*>(ws);
+    a.status = status;
+
+    const size_t smem = static_cast<size_t>(E) * sizeof(int32_t);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !g_smem_attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kMaxExperts * static_cast<int>(sizeof(int32_t)));
+        if (err != cudaSuccess) return cuda_fail(err);
+        g_smem_attr_set[dev] = true;
+    }
+    layout_kernel<<<a.num_tiles, kTileTokens, smem, as_stream(stream)>>>(a);
+    return check_launch();
+}

@@ -1,0 +1,238 @@
+/*
+ * ep.h -- C ABI of the GB300 (sm_103a) expert-parallel dispatch/combine library.
+ *
+ * One GPU holds R "virtual" expert-parallel ranks as partitions of its HBM: a
+ * rank's receive buffer is its slab [max_tokens][...] of a destination-major
+ * [R][max_tokens][...] array. Sending a token to a rank is a store into that
+ * slab; receiving is a load from it. The operations follow the expert-parallel
+ * dispatch/combine described on the DeepEP pull-request pages:
+ *   [PR #347] "Feature/sm free normal kernel" (sections 2.1 Feature,
+ *     3.1 Experiment Setup, 3.2.1 tables, 3.3.1 HBM Cost; the commit that adds
+ *     return_recv_hook to get_dispatch_layout),
+ *   [PR #634] "Hybrid ep nixl restripe" (sections Baseline problem, Fix,
+ *     Receive-side and DOCA path are unchanged; the scan permute-fusion commit),
+ *   [PR #453] "Higher Performance with Lower SM Occupancy through Zero-Copy and
+ *     TMA Offloading" (commits: recv-count assertion, separate dispatch/combine
+ *     buffer sizes, buffer alignment).
+ *
+ * General contract (every entry point):
+ *   - Pointers named d_* / device arrays are CUDA device pointers on the
+ *     current device; the library reads and writes them only from kernels
+ *     launched on `stream`. The caller owns every buffer; the library never
+ *     allocates, frees or synchronises, and returns as soon as its kernels are
+ *     queued.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Arrays are dense, row-major, in the layout stated per argument. Every
+ *     array pointer must be 16-byte aligned (rows are moved in 16-byte vectors).
+ *   - Sizes are int32; products of sizes are computed in 64 bits.
+ *   - The return value is synchronous: EP_OK when the kernels were queued,
+ *     EP_ERR_INVALID when an argument is rejected (nothing was launched),
+ *     EP_ERR_CUDA when a launch failed (ep_last_cuda_error() gives the code).
+ *   - Errors found by the kernels are reported asynchronously by OR-ing
+ *     EP_FLAG_* bits into `*status` (a device int32, zeroed by the caller;
+ *     status may be NULL to ignore them). Kernels never trap: an out-of-range
+ *     write is skipped, never performed.
+ *   - Calls on one stream run in order; two calls that share an output or a
+ *     workspace must not run concurrently on different streams.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EP_ABI_VERSION 1
+
+typedef int32_t ep_status_t;
+#define EP_OK 0
+#define EP_ERR_INVALID 1
+#define EP_ERR_CUDA 2
+
+/* asynchronous error bits OR-ed into *status by the kernels */
+#define EP_FLAG_CAPACITY 1   /* a receive slot >= max_tokens was dropped ([PR #453] commit
+                                "Add assertion against too large recv token count", as a flag) */
+#define EP_FLAG_BAD_EXPERT 2 /* a topk_idx entry >= E was skipped */
+#define EP_FLAG_TIMEOUT 4    /* a bounded wait of the layout scan gave up */
+#define EP_FLAG_WORKSPACE 8  /* the layout workspace was not at rest: zero-fill it and call again */
+
+typedef int32_t ep_dtype_t;
+#define EP_DTYPE_BF16 0 /* bfloat16 rows, 2 bytes per element */
+#define EP_DTYPE_E4M3 1 /* OCP E4M3 rows (1 byte per element) + one fp32 scale per 128 elements */
+
+typedef int32_t ep_node_mode_t;
+#define EP_NODES_DENSE 0  /* copy every chunk's whole token range to every node */
+#define EP_NODES_SPARSE 1 /* copy only the runs of consecutive tokens routed to the node */
+
+/* ABI version of the loaded library (EP_ABI_VERSION at build time). */
+int32_t ep_abi_version(void);
+
+/* Static string describing a synchronous status (EP_OK, EP_ERR_*). Never NULL. */
+const char* ep_status_str(ep_status_t s);
+
+/* cudaError_t code behind the most recent EP_ERR_CUDA returned on the calling
+ * host thread (0 if there was none). */
+int32_t ep_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------- */
+/* Routing layout                                                            */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of device workspace ep_get_layout needs for these sizes. */
+size_t ep_layout_workspace_size(int32_t T, int32_t E, int32_t R, int32_t ranks_per_node);
+
+/* First bytes of the layout workspace. The workspace must be zero-filled once
+ * before its first use; every completed call leaves it ready for the next call
+ * (the counters return to zero and the epoch advances). `stall_tile` is a test
+ * hook: when it holds i + 1, tile i never publishes its counts, so that the
+ * bounded waits of its successors run out and raise EP_FLAG_TIMEOUT. Keep it 0. */
+typedef struct {
+    uint32_t ticket;     /* next tile index handed out */
+    uint32_t done;       /* tiles finished */
+    uint32_t epoch;      /* calls completed on this workspace */
+    uint32_t stall_tile; /* test hook, 0 = off */
+} ep_layout_ws_header_t;
+
+/* ep_get_layout -- the routing layout of a batch (get_dispatch_layout,
+ * [PR #347] commit list; the scan of [PR #634] "fix scan permute-fusion
+ * local-experts sum array sizing").
+ *
+ * Inputs
+ *   topk_idx        int64 [T][k]  router output: expert ids; < 0 = no expert;
+ *                                 >= E is skipped and raises EP_FLAG_BAD_EXPERT
+ *   T >= 0 tokens, 1 <= k <= 32, 1 <= R <= 256 ranks, E experts with E % R == 0
+ *   and E <= 8192 (expert e lives on rank e / (E/R)); ranks_per_node = 0 (no
+ *   node outputs) or a divisor of R (rank r lives on node r / ranks_per_node).
+ * Outputs (all overwritten, in token order)
+ *   tokens_per_expert int32 [E]   number of (t, j) with topk_idx[t][j] == e
+ *   tokens_per_rank   int32 [R]   tokens sent to each rank (a token with several
+ *                                 experts on one rank is sent once)
+ *   tokens_per_node   int32 [N]   likewise per node (NULL when ranks_per_node = 0)
+ *   is_token_in_rank  uint8 [T][R] 1 when token t goes to rank r
+ *   is_token_in_node  uint8 [T][N] likewise per node (NULL when ranks_per_node = 0)
+ *   slot              int32 [T][R] stable exclusive prefix sum down the tokens:
+ *                                 #{t' < t : is_token_in_rank[t'][r]}, or -1
+ *   workspace         device, >= ep_layout_workspace_size(...) bytes, 256-byte
+ *                     aligned, zero-filled before its first use (see above)
+ *   status            device int32 or NULL; EP_FLAG_BAD_EXPERT, EP_FLAG_TIMEOUT,
+ *                     EP_FLAG_WORKSPACE (outputs not written)
+ */
+ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E, int32_t R,
+                          int32_t ranks_per_node, int32_t* tokens_per_expert,
+                          int32_t* tokens_per_rank, int32_t* tokens_per_node,
+                          uint8_t* is_token_in_rank, uint8_t* is_token_in_node, int32_t* slot,
+                          void* workspace, size_t workspace_bytes, int32_t* status,
+                          void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Rank-level dispatch                                                       */
+/* ------------------------------------------------------------------------- */
+
+/* ep_dispatch -- send every token once to every rank it routes to ([PR #347]
+ * 2.1 Feature; workload of 3.1: 4096 tokens, hidden 7168, top-8; FP8 and BF16
+ * dispatch of 3.2.1). For every (t, r) with s = slot[t][r] >= 0:
+ *   recv_x[r][s][:]        = x[t][:]                  (out_dtype BF16), or
+ *                            e4m3(x[t][:] / scale_b)  (out_dtype E4M3) with
+ *   recv_scales[r][s][b]   = scale_b = amax_b / 448, amax_b = max |x| over the
+ *                            128 elements of block b (fp32, correctly rounded
+ *                            division; q rounded once to nearest-even and
+ *                            saturated to +-448; a block with amax 0 stores
+ *                            scale 0 and the signed zero code of each element)
+ *   recv_src_idx[r][s]     = t
+ *   recv_topk_idx[r][s][j] = e_j - r*(E/R) when expert e_j lives on r, else -1
+ *   recv_topk_w[r][s][j]   = topk_w[t][j] when expert e_j lives on r, else 0
+ * A slot >= max_tokens is dropped and raises EP_FLAG_CAPACITY. Rows a rank does
+ * not receive are not written.
+ *
+ *   x             bf16 [T][H], H % 8 == 0 (H % 128 == 0 for E4M3)
+ *   topk_idx      int64 [T][k], topk_w fp32 [T][k] (topk_w may be NULL when
+ *                 recv_topk_w is NULL)
+ *   slot          int32 [T][R] from ep_get_layout
+ *   recv_x        [R][max_tokens][H] of out_dtype           (required)
+ *   recv_scales   fp32 [R][max_tokens][H/128]               (E4M3 only, else NULL)
+ *   recv_src_idx  int32 [R][max_tokens]                     (nullable)
+ *   recv_topk_idx int32 [R][max_tokens][k]                  (nullable)
+ *   recv_topk_w   fp32 [R][max_tokens][k]                   (nullable)
+ *   status        EP_FLAG_CAPACITY, EP_FLAG_BAD_EXPERT
+ */
+ep_status_t ep_dispatch(const void* x, ep_dtype_t out_dtype, const int64_t* topk_idx,
+                        const float* topk_w, const int32_t* slot, int32_t T, int32_t H, int32_t k,
+                        int32_t E, int32_t R, int32_t max_tokens, void* recv_x,
+                        float* recv_scales, int32_t* recv_src_idx, int32_t* recv_topk_idx,
+                        float* recv_topk_w, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Prob restripe                                                             */
+/* ------------------------------------------------------------------------- */
+
+/* ep_restripe_prob -- [PR #634] "Baseline problem" / "Fix": copy the prob
+ * tensor from its token-major layout [T][num_nodes][P] into the
+ * destination-major staging layout [num_nodes][max_tokens][P], so that the
+ * slices one destination needs for consecutive tokens are contiguous:
+ *   out[n][t][p] = prob[t][n][p]   for all t < T, n < num_nodes, p < P.
+ * Every (t, n) slice is copied (the same bytes as the plain copy it replaces);
+ * rows t in [T, max_tokens) are not written.
+ *   prob  fp32 [T][num_nodes][P], P % 4 == 0;  out fp32 [num_nodes][max_tokens][P]
+ *   requires T <= max_tokens.
+ */
+ep_status_t ep_restripe_prob(const float* prob, int32_t T, int32_t num_nodes, int32_t P,
+                             int32_t max_tokens, float* out, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Node-level dense / sparse dispatch                                        */
+/* ------------------------------------------------------------------------- */
+
+/* ep_dispatch_nodes -- [PR #634] "Fix": per chunk of chunk_tokens consecutive
+ * tokens (NUM_OF_TOKENS_PER_CHUNK = 256 on the page) and destination node n,
+ *   EP_NODES_DENSE : the chunk's whole token range of hidden rows and of staged
+ *                    prob slices goes to n in one contiguous copy each;
+ *   EP_NODES_SPARSE: only the maximal runs of consecutive tokens of the chunk
+ *                    with is_token_in_node[t][n] go, one copy per run.
+ * The receive layout is token-indexed (destination positions follow source
+ * positions; the receive side keeps token-major strides, [PR #634] "Receive-side
+ * and DOCA path are unchanged"):
+ *   recv_x_node[n][t][:]    = x[t][:]
+ *   recv_prob_node[n][t][:] = prob_staging[n][t][:]
+ *   num_runs[n][c]          = copies of hidden rows made for (n, chunk c):
+ *                             1 per non-empty chunk (dense), runs (sparse)
+ *   x bf16 [T][H] (H % 8 == 0); prob_staging fp32 [num_nodes][max_tokens][P]
+ *   from ep_restripe_prob (P % 4 == 0; NULL together with recv_prob_node to
+ *   move rows only); is_token_in_node uint8 [T][num_nodes] from ep_get_layout
+ *   (read on the sparse path only; may be NULL on the dense path);
+ *   recv_x_node bf16 [num_nodes][max_tokens][H]; recv_prob_node fp32
+ *   [num_nodes][max_tokens][P]; num_runs int32 [num_nodes][ceil(T/chunk_tokens)]
+ *   or NULL. Requires T <= max_tokens, chunk_tokens >= 1.
+ */
+ep_status_t ep_dispatch_nodes(const void* x, const float* prob_staging,
+                              const uint8_t* is_token_in_node, int32_t T, int32_t H,
+                              int32_t num_nodes, int32_t P, int32_t max_tokens,
+                              int32_t chunk_tokens, ep_node_mode_t mode, void* recv_x_node,
+                              float* recv_prob_node, int32_t* num_runs, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Combine                                                                   */
+/* ------------------------------------------------------------------------- */
+
+/* ep_combine -- bring every rank's expert output for a token back to the
+ * token's position and reduce ([PR #347] 2.1 Feature; BF16 combine of 3.2.1):
+ *   out[t][h] = bf16_rn( sum over r = 0, 1, ..., R-1 ascending with
+ *                        s = slot[t][r] >= 0 of float(y[r][s][h]) )
+ * accumulated in fp32 from +0 in exactly that order (one IEEE addition per
+ * term, one rounding to bf16 at the end), so the result is deterministic. The
+ * sum is unweighted: top-k weights belong to the expert. A token routed
+ * nowhere gets +0. A slot >= max_tokens was never received: it is skipped and
+ * raises EP_FLAG_CAPACITY.
+ *   y    bf16 [R][max_tokens][H], H % 8 == 0
+ *   slot int32 [T][R] from ep_get_layout
+ *   out  bf16 [T][H]
+ */
+ep_status_t ep_combine(const void* y, const int32_t* slot, int32_t T, int32_t H, int32_t R,
+                       int32_t max_tokens, void* out, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EP_GB300_H */

@@ -1,0 +1,315 @@
+"""GPU parity: the CUDA library against the oracle, element by element, on the
+same seeded inputs (workloads.py). Layout, dispatch (bf16 and E4M3), restripe
+and node dispatch must be bit-exact; combine sums in ascending rank order, so
+it must be bit-exact too. Every output buffer sits between guard regions that
+must be unchanged afterwards, and rows a rank does not receive must keep their
+sentinel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_get_05_gb300 as ep
+import oracle
+import workloads
+from gpu_helpers import (SENT_BF16, SENT_F32, SENT_I32, check_guards, dev_bf16, gpu_expert, gpu_layout, guarded,
+                         host_bits, layout_to_host, oracle_expert)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ep.build_library()
+    ep.lib()
+
+
+def _max_tokens(w, L):
+    return w.max_tokens if w.max_tokens is not None else max(1, int(L["tokens_per_rank"].max()))
+
+
+def _assert_layout(w, lay, L):
+    got = layout_to_host(lay)
+    for key, v in got.items():
+        assert np.array_equal(v, L[key]), key
+    assert ep.read_flags(lay.status) == L["flags"]
+
+
+def run_rank_path(w, max_tokens=None, full_compare=True):
+    """Layout -> dispatch -> harness expert -> combine on both sides; compare everything."""
+    L = oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node)
+    M = max_tokens if max_tokens is not None else _max_tokens(w, L)
+    topk, lay = gpu_layout(w)
+    _assert_layout(w, lay, L)
+
+    x = dev_bf16(w.x)
+    tw = torch.from_numpy(w.topk_w).cuda()
+    H, R, k, fp8 = w.H, w.R, w.k, w.fp8
+    fill_x = 0xAB if fp8 else SENT_BF16
+    recv_x, bx = guarded((R, M, H), torch.uint8 if fp8 else torch.bfloat16, fill_x)
+    recv_scales, bs = guarded((R, M, H // 128), torch.float32, SENT_F32) if fp8 else (None, None)
+    src, bsrc = guarded((R, M), torch.int32, SENT_I32)
+    tidx, btidx = guarded((R, M, k), torch.int32, SENT_I32)
+    tww, btw = guarded((R, M, k), torch.float32, SENT_F32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_dispatch(x, ep.DTYPE_E4M3 if fp8 else ep.DTYPE_BF16, topk, tw, lay.slot, w.E, R, M, recv_x, recv_scales,
+                   src, tidx, tww, status)
+    D = oracle.dispatch(w.x, w.topk_idx, w.topk_w, L["slot"], w.E, R, M, fp8=fp8, rows=full_compare,
+                        fill_x=fill_x, fill_idx=SENT_I32, fill_w=SENT_F32)
+    assert ep.read_flags(status) == D["flags"]
+    assert np.array_equal(host_bits(src), D["recv_src_idx"])
+    assert np.array_equal(host_bits(tidx), D["recv_topk_idx"])
+    assert np.array_equal(host_bits(tww).view(np.uint32), D["recv_topk_w"].view(np.uint32))
+    guards = [(bx, recv_x, fill_x), (bsrc, src, SENT_I32), (btidx, tidx, SENT_I32), (btw, tww, SENT_F32)]
+    if fp8:
+        guards.append((bs, recv_scales, SENT_F32))
+    for backing, view, fill in guards:
+        check_guards(backing, view.numel(), fill)
+    if full_compare:
+        assert np.array_equal(host_bits(recv_x), D["recv_x"])
+        if fp8:
+            assert np.array_equal(host_bits(recv_scales).view(np.uint32), D["recv_scales"].view(np.uint32))
+
+    # harness expert on each side, then combine
+    y = recv_x if (w.expert == "identity" and not fp8) else gpu_expert(recv_x, tww, recv_scales)
+    out, bout = guarded((w.T, H), torch.bfloat16, SENT_BF16)
+    cstatus = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_combine(y, lay.slot, M, out, cstatus)
+    torch.cuda.synchronize()
+    check_guards(bout, out.numel(), SENT_BF16)
+    if full_compare:
+        Y = oracle_expert(w, D, L)
+        received = np.arange(M)[None, :] < np.minimum(L["tokens_per_rank"], M)[:, None]  # [R][M]
+        assert np.array_equal(host_bits(y)[received], Y[received])
+        ref, cflags = oracle.combine(Y, L["slot"], M)
+        assert ep.read_flags(cstatus) == cflags
+        assert np.array_equal(host_bits(out), ref)
+    return L, host_bits(out)
+
+
+# ----------------------------------------------------------------------------- whole path
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", {}),
+    ("tiny", {"T": 1}),
+    ("tiny", {"T": 257, "H": 8}),
+    ("dsv3", {"T": 1000, "H": 1024}),
+    ("dsv3", {"T": 777, "H": 7168}),
+    ("dsv3_fp8", {"T": 1000, "H": 1024}),
+    ("dsv3_fp8", {"T": 333, "H": 384}),
+    ("skewed", {"T": 2000, "H": 256}),
+    ("restripe", {"T": 700, "H": 512}),
+])
+def test_rank_path_matches_oracle(name, over):
+    run_rank_path(workloads.make(name, **over))
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "dsv3_fp8"])
+def test_rank_path_full_size(name):
+    """The full workloads, as the benchmark launches them, compared in full."""
+    run_rank_path(workloads.make(name))
+
+
+def test_capacity_overflow_drops_and_flags():
+    w = workloads.make("skewed", T=3000, H=128)
+    L = oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node)
+    run_rank_path(w, max_tokens=int(L["tokens_per_rank"].max()) // 2)
+
+
+def test_bad_expert_ids_are_skipped_and_flagged():
+    w = workloads.make("tiny", T=200)
+    w.topk_idx[5, 1] = w.E + 3
+    w.topk_idx[77, 0] = 10 ** 9
+    w.topk_idx[100, :] = -1  # routed nowhere: combine gives +0
+    run_rank_path(w)
+
+
+def test_duplicate_experts_on_one_rank_and_all_to_one_rank():
+    w = workloads.make("tiny", T=300, H=64)
+    w.topk_idx[:] = np.array([0, 1, 2, 3], np.int64)  # every token: four experts, all on rank 0
+    run_rank_path(w)
+
+
+@pytest.mark.parametrize("R,E,k", [(1, 8, 3), (256, 256, 8), (64, 8192, 32), (7, 21, 2)])
+def test_rank_path_extreme_shapes(R, E, k):
+    rng = np.random.Generator(np.random.PCG64(R * 1000 + k))
+    T, H = 300, 64
+    w = workloads.make("tiny", T=T, H=H, E=E, k=k, R=R, ranks_per_node=R)
+    w.topk_idx = workloads.routing_uniform(rng, T, E, k)
+    w.topk_w = rng.random((T, k), dtype=np.float32)
+    w.expert = "scale"
+    run_rank_path(w)
+
+
+def test_full_size_skewed_sampled():
+    """T=16384, H=4096, R=64, max_tokens sized to the hottest rank: metadata in full,
+    rows and combine outputs on sampled tokens."""
+    w = workloads.make("skewed")
+    L = oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node)
+    M = _max_tokens(w, L)
+    topk, lay = gpu_layout(w)
+    _assert_layout(w, lay, L)
+    x = dev_bf16(w.x)
+    tw = torch.from_numpy(w.topk_w).cuda()
+    d = ep.alloc_dispatch(w.R, M, w.H, w.k)
+    ep.dispatch(x, topk, tw, lay, M, out=d)
+    D = oracle.dispatch(w.x, w.topk_idx, w.topk_w, L["slot"], w.E, w.R, M, rows=False, fill_idx=SENT_I32,
+                        fill_w=SENT_F32)
+    cnt = np.minimum(L["tokens_per_rank"], M)
+    valid = np.arange(M)[None, :] < cnt[:, None]
+    assert np.array_equal(host_bits(d.recv_src_idx)[valid], D["recv_src_idx"][valid])
+    assert np.array_equal(host_bits(d.recv_topk_idx)[valid], D["recv_topk_idx"][valid])
+    assert np.array_equal(host_bits(d.recv_topk_w)[valid], D["recv_topk_w"][valid])
+    rng = np.random.Generator(np.random.PCG64(99))
+    rs = rng.integers(0, w.R, 3000)
+    ss = (rng.random(3000) * cnt[rs]).astype(np.int64)
+    rows = host_bits(d.recv_x[torch.from_numpy(rs).cuda(), torch.from_numpy(ss).cuda()])
+    assert np.array_equal(rows, w.x[D["recv_src_idx"][rs, ss]])
+    # combine: the oracle pipeline on the sub-batch of sampled tokens gives their rows exactly
+    y = gpu_expert(d.recv_x, d.recv_topk_w)
+    out = ep.combine(y, lay, M)
+    tok = np.sort(rng.choice(w.T, 512, replace=False))
+    Ls = oracle.layout(w.topk_idx[tok], w.E, w.R)
+    Ds = oracle.dispatch(w.x[tok], w.topk_idx[tok], w.topk_w[tok], Ls["slot"], w.E, w.R, len(tok))
+    Ys = oracle.expert_scale(Ds["recv_x"], Ds["recv_topk_w"], Ls["tokens_per_rank"])
+    ref, _ = oracle.combine(Ys, Ls["slot"], len(tok))
+    assert np.array_equal(host_bits(out)[tok], ref)
+    assert ep.read_flags(lay.status) == 0 and ep.read_flags(d.status) == 0
+
+
+# ----------------------------------------------------------------------------- FP8 rounding edges
+
+def test_fp8_ties_subnormals_and_signed_zeros():
+    """Blocks with amax = 448 (scale exactly 1) whose other elements sit on E4M3 midpoints
+    (normal and subnormal), plus an all-zero block with -0 entries."""
+    mids = []
+    vals = sorted({oracle.e4m3_to_f32(c) for c in range(0x7F) if c != 0x7F})
+    for a, b in zip(vals[:-1], vals[1:]):
+        mids.append((a + b) / 2)
+    mids = np.array(mids, np.float32)
+    rows = []
+    rng = np.random.Generator(np.random.PCG64(21))
+    for i in range(6):
+        blocks = []
+        for b in range(4):
+            v = rng.choice(mids, 128).astype(np.float32) * rng.choice(np.array([-1, 1], np.float32), 128)
+            v[rng.integers(0, 128)] = 448.0 * (1 if b % 2 == 0 else -1)
+            blocks.append(v)
+        if i == 3:
+            blocks[2] = np.zeros(128, np.float32)
+            blocks[2][::3] = -0.0
+        rows.append(np.concatenate(blocks))
+    xf = np.stack(rows).astype(np.float32)
+    bits = workloads.bf16_bits(xf)
+    back = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    assert np.array_equal(back, xf)  # E4M3 midpoints are exact in bf16
+    T, H = bits.shape
+    w = workloads.make("tiny", T=T, H=H, E=4, k=1, R=4)
+    w.x = bits
+    w.topk_idx = np.arange(T, dtype=np.int64)[:, None] % 4
+    w.topk_w = np.ones((T, 1), np.float32)
+    w.fp8 = True
+    w.expert = "scale"
+    run_rank_path(w)
+
+
+def test_combine_order_crafted():
+    """2^24, 1, -2^24 from ranks 0, 1, 2: ascending fp32 order gives 0, descending 1."""
+    H, R = 64, 3
+    y = np.stack([workloads.bf16_bits(np.full((1, H), v, np.float32)) for v in (2.0 ** 24, 1.0, -(2.0 ** 24))])
+    slot = np.zeros((1, R), np.int32)
+    out = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine(dev_bf16(y), torch.from_numpy(slot).cuda(), 1, out)
+    ref, _ = oracle.combine(y, slot, 1)
+    assert np.array_equal(host_bits(out), ref)
+    assert np.all(ref == 0)
+
+
+# ----------------------------------------------------------------------------- restripe + node dispatch
+
+def run_node_path(w, chunk=None, P_override=None):
+    chunk = chunk or w.chunk_tokens
+    L = oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node)
+    topk, lay = gpu_layout(w)
+    _assert_layout(w, lay, L)
+    N, T, M, H = w.num_nodes, w.T, w.max_tokens, w.H
+    prob = torch.from_numpy(w.prob).cuda()
+    P = w.prob.shape[2]
+    staging, bst = guarded((N, M, P), torch.float32, SENT_F32)
+    ep.ep_restripe_prob(prob, M, staging)
+    ref_st = oracle.restripe_prob(w.prob, M, fill=SENT_F32)
+    assert np.array_equal(host_bits(staging).view(np.uint32), ref_st.view(np.uint32))
+    check_guards(bst, staging.numel(), SENT_F32)
+    x = dev_bf16(w.x)
+    nchunks = (T + chunk - 1) // chunk
+    for mode, dense in ((ep.NODES_DENSE, True), (ep.NODES_SPARSE, False)):
+        rx, brx = guarded((N, M, H), torch.bfloat16, SENT_BF16)
+        rp, brp = guarded((N, M, P), torch.float32, SENT_F32)
+        runs = torch.full((N, nchunks), SENT_I32, dtype=torch.int32, device="cuda")
+        ep.ep_dispatch_nodes(x, staging, lay.is_token_in_node, N, M, chunk, mode, rx, rp, runs)
+        ref = oracle.dispatch_nodes(w.x, ref_st, L["is_token_in_node"], M, chunk, dense=dense, fill_x=SENT_BF16,
+                                    fill_prob=SENT_F32)
+        assert np.array_equal(host_bits(rx), ref["recv_x_node"])
+        assert np.array_equal(host_bits(rp).view(np.uint32), ref["recv_prob_node"].view(np.uint32))
+        assert np.array_equal(host_bits(runs), ref["num_runs"])
+        check_guards(brx, rx.numel(), SENT_BF16)
+        check_guards(brp, rp.numel(), SENT_F32)
+
+
+@pytest.mark.parametrize("over,chunk", [
+    ({"T": 700, "H": 512}, 256),
+    ({"T": 1000, "H": 64, "P": 4}, 100),
+    ({"T": 33, "H": 8, "P": 8, "N": 1, "ranks_per_node": 2}, 7),
+    ({"T": 4097, "H": 128, "P": 128, "N": 16, "ranks_per_node": 2}, 256),
+    ({"T": 600, "H": 256, "max_tokens": 1000}, 64),
+])
+def test_node_path_matches_oracle(over, chunk):
+    run_node_path(workloads.make("restripe", **over), chunk=chunk)
+
+
+def test_node_path_full_size():
+    """T=8192, H=7168, 8 nodes, P=128, chunks of 256: restripe, dense and sparse, in full."""
+    run_node_path(workloads.make("restripe"))
+
+
+# ----------------------------------------------------------------------------- layout specifics
+
+def test_layout_empty_batch_and_workspace_reuse():
+    lay = ep.alloc_layout(5000, 256, 32, 4)
+    for T in (0, 1, 300, 5000, 17, 4096):
+        w = workloads.make("dsv3", T=T if T else 1, H=8)
+        topk = torch.from_numpy(w.topk_idx[:T]).cuda()
+        sub = ep.Layout(lay.tokens_per_expert, lay.tokens_per_rank, lay.tokens_per_node,
+                        lay.is_token_in_rank[:T], lay.is_token_in_node[:T], lay.slot[:T], lay.workspace, lay.status,
+                        256, 32, 4)
+        ep.get_layout(topk, 256, 32, 4, out=sub)
+        L = oracle.layout(w.topk_idx[:T], 256, 32, 4)
+        got = layout_to_host(sub)
+        for key, v in got.items():
+            assert np.array_equal(v, L[key]), (T, key)
+    assert ep.read_flags(lay.status) == 0
+
+
+def test_layout_bounded_wait_times_out_without_hanging():
+    """Tile 1 never publishes (test hook): its successors give up after about a second,
+    raise EP_FLAG_TIMEOUT, and the workspace still works for the next call."""
+    w = workloads.make("dsv3", T=256 * 6, H=8)
+    topk = torch.from_numpy(w.topk_idx).cuda()
+    lay = ep.alloc_layout(w.T, w.E, w.R, w.ranks_per_node)
+    lay.workspace[12:16].copy_(torch.tensor([2, 0, 0, 0], dtype=torch.uint8))  # stall_tile = 1 + 1
+    ep.get_layout(topk, w.E, w.R, w.ranks_per_node, out=lay)
+    assert ep.read_flags(lay.status) & ep.FLAG_TIMEOUT
+    lay.workspace[12:16].zero_()
+    lay.status.zero_()
+    ep.get_layout(topk, w.E, w.R, w.ranks_per_node, out=lay)
+    L = oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node)
+    _assert_layout(w, lay, L)
+
+
+def test_outputs_are_deterministic():
+    w = workloads.make("dsv3", T=2048, H=2048)
+    _, a = run_rank_path(w)
+    _, b = run_rank_path(w)
+    assert np.array_equal(a, b)

@@ -233,6 +233,21 @@ def cpu_baseline(w, budget_s=12.0, tokens=None):
 
 # --------------------------------------------------------------------------- GPU arm
 
+def capture(fn, warm=2):
+    """Capture fn (library launches on the current stream) into a CUDA graph."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warm):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def run_ours(args, world, rank):
     import combine_ep_get_05_gb300 as ep
 
@@ -252,49 +267,71 @@ def run_ours(args, world, rank):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def do_layout():
         ep.get_layout(topk, E, R, rpn, out=lay)
+
+    def do_dispatch():
         ep.dispatch(x, topk, tw, lay, M, out=disp)
+
+    def do_combine():
         ep.combine(disp.recv_x, lay, M, out=out, status=cstatus)
+
+    def step():
+        do_layout()
+        do_dispatch()
+        do_combine()
+
+    step()
+    torch.cuda.synchronize()
+    g_step = capture(step)
+    g_stage = {"layout": capture(do_layout), "dispatch": capture(do_dispatch), "combine": capture(do_combine)}
 
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        g_step.replay()
     torch.cuda.synchronize()
     pairs = int(lay.tokens_per_rank.sum().item())
     flags = ep.read_flags(lay.status) | ep.read_flags(disp.status) | ep.read_flags(cstatus)
     if flags:
         raise RuntimeError(f"kernels raised status flags {flags}")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     clocks = ClockSampler(dev.index)
     clocks.start()
-    time.sleep(0.3)
+    soak_end = time.perf_counter() + args.soak_s  # untimed load so the sampled clocks are under load
+    while time.perf_counter() < soak_end:
+        for _ in range(20):
+            flush.zero_()
+            g_step.replay()
+        torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for a, z in ev:
         flush.zero_()
-        e = ev[i]
-        e[0].record(stream)
-        ep.get_layout(topk, E, R, rpn, out=lay)
-        e[1].record(stream)
-        ep.dispatch(x, topk, tw, lay, M, out=disp)
-        e[2].record(stream)
-        ep.combine(disp.recv_x, lay, M, out=out, status=cstatus)
-        e[3].record(stream)
+        a.record(stream)
+        g_step.replay()
+        z.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
-    clk = clocks.stop()
+    step_ms = [a.elapsed_time(z) for a, z in ev]
 
-    stage_ms = {"layout": [], "dispatch": [], "combine": []}
-    step_ms = []
-    for e in ev:
-        stage_ms["layout"].append(e[0].elapsed_time(e[1]))
-        stage_ms["dispatch"].append(e[1].elapsed_time(e[2]))
-        stage_ms["combine"].append(e[2].elapsed_time(e[3]))
-        step_ms.append(e[0].elapsed_time(e[3]))
+    # per-kernel durations: each stage's graph alone, L2 flushed before it
+    stage_ms = {s: [] for s in g_stage}
+    for _ in range(args.steps):
+        for s, g in g_stage.items():
+            flush.zero_()
+            a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            z.record(stream)
+            stage_ms[s].append((a, z))
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    stage_ms = {s: [a.elapsed_time(z) for a, z in v] for s, v in stage_ms.items()}
+
     ms = max_over_ranks(world, statistics.mean(step_ms))
     b = step_bytes(T, H, k, E, R, N, pairs)
     total_bytes = sum(b.values())
@@ -306,20 +343,56 @@ def run_ours(args, world, rank):
     dom_src = {"dispatch": "ep_dispatch.cu", "combine": "ep_combine.cu"}[dom]
     achieved = b[dom] / (mean[dom] * 1e-3) / 1e9
     traffic, traffic_note = committed_traffic(dom_kernel, dom_src)
-
     stages = {s: {"ms": round(mean[s], 4), "ms_p10": round(float(np.percentile(stage_ms[s], 10)), 4),
                   "ms_p90": round(float(np.percentile(stage_ms[s], 90)), 4),
                   "alg_bytes": b[s], "gbs": round(b[s] / (mean[s] * 1e-3) / 1e9, 1),
                   "frac_of_hbm_peak": round(b[s] / (mean[s] * 1e-3) / 1e9 / peak, 4)} for s in stage_ms}
 
-    # ----- end to end through the public API with pinned host buffers
+    e2e = None if args.no_e2e else run_e2e(ep, w, dev, lay, disp, out, cstatus, flush, args, world, total_bytes)
+    extra = {} if args.skip_extra else extra_stages(ep, dev, args, flush, peak)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "dsv3 prefill: T=4096 H=7168 bf16, E=256 top-8, R=32 virtual ranks "
+                               "(8 nodes x 4), max_tokens=4096, identity expert",
+                   "T": T, "H": H, "E": E, "k": k, "R": R, "nodes": N, "max_tokens": M,
+                   "pairs": pairs, "parallelism": f"replicas x{world}",
+                   "launch": "each step is one CUDA graph replay of the three library kernels",
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "soak_s": args.soak_s},
+        "tokens_per_s": round(world * T / (ms * 1e-3), 1),
+        "frac_of_hbm_peak": round(value / world / peak, 4),
+        "stages": stages,
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} (copy bandwidth, hbm_gbs)"
+                     if peak_kind == "measured" else "fallback", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "alg_bytes_per_launch": b[dom], "traffic_note": traffic_note},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+        "extra_workloads": extra,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    return line
+
+
+def run_e2e(ep, w, dev, lay, disp, out, cstatus, flush, args, world, total_bytes):
+    """The same step through the public API as a user calls it, with the inputs copied in
+    from pinned host memory and the combined result copied back, every step."""
+    T, H, E, R, rpn, M = w.T, w.H, w.E, w.R, w.ranks_per_node, w.max_tokens
+    stream = torch.cuda.current_stream()
     x_h = torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16).pin_memory()
     topk_h = torch.from_numpy(w.topk_idx).pin_memory()
     tw_h = torch.from_numpy(w.topk_w).pin_memory()
     out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(x)
-    topk_d = torch.empty_like(topk)
-    tw_d = torch.empty_like(tw)
+    x_d = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    topk_d = torch.empty_like(topk_h, device=dev)
+    tw_d = torch.empty_like(tw_h, device=dev)
 
     def e2e_step():
         x_d.copy_(x_h, non_blocking=True)
@@ -342,50 +415,23 @@ def run_ours(args, world, rank):
         z.record(stream)
         z.synchronize()
         e2e_ms.append(a.elapsed_time(z))
-    torch.cuda.synchronize()
     assert torch.equal(out_h, out.cpu())
-    e2e_t = max_over_ranks(world, statistics.mean(e2e_ms))
-    h2d = x_h.numel() * 2 + topk_h.numel() * 8 + tw_h.numel() * 4
-    d2h = out_h.numel() * 2
-
-    extra = {} if args.skip_extra else extra_stages(ep, dev, args, flush, peak)
-
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "dsv3 prefill: T=4096 H=7168 bf16, E=256 top-8, R=32 virtual ranks "
-                               "(8 nodes x 4), max_tokens=4096, identity expert",
-                   "T": T, "H": H, "E": E, "k": k, "R": R, "nodes": N, "max_tokens": M,
-                   "pairs": pairs, "parallelism": f"replicas x{world}",
-                   "l2": "flushed between steps (256 MiB write outside the timed events)"},
-        "tokens_per_s": round(world * T / (ms * 1e-3), 1),
-        "frac_of_hbm_peak": round(value / world / peak, 4),
-        "stages": stages,
-        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(achieved, 1),
-                     "peak": peak, "peak_kind": f"{peak_kind} (copy, MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "alg_bytes_per_launch": b[dom], "traffic_note": traffic_note},
-        "e2e": {"value": round(world * total_bytes / (e2e_t * 1e-3) / 1e9, 2), "unit": UNIT,
-                "ms_per_step": round(e2e_t, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
-        "clocks": clk,
-        "wall_s_timed_region": round(wall, 4),
-        "extra_workloads": extra,
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
-    return line
+    t = max_over_ranks(world, statistics.mean(e2e_ms))
+    return {"value": round(world * total_bytes / (t * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(t, 4),
+            "h2d_bytes_per_step": x_h.numel() * 2 + topk_h.numel() * 8 + tw_h.numel() * 4,
+            "d2h_bytes_per_step": out_h.numel() * 2,
+            "path": "pinned host -> cudaMemcpyAsync -> ep_get_layout, ep_dispatch, ep_combine -> pinned host"}
 
 
 def time_events(fn, n, flush, stream):
+    """Mean device time of fn, captured in a CUDA graph, L2 flushed before each replay."""
+    g = capture(fn)
     ms = []
     for _ in range(n):
         flush.zero_()
         a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        fn()
+        g.replay()
         z.record(stream)
         ms.append((a, z))
     torch.cuda.synchronize()
@@ -504,6 +550,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--skip-extra", action="store_true", help="skip the other workloads' stage timings")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
+    ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed steps (clocks)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         log("warmup raised to 3 (minimum)")

@@ -247,12 +247,19 @@ bool g_smem_attr_set[64] = {};
 
 }  // namespace
 
+// Workspace layout: [header | expert accumulators (kMaxExperts) | node accumulators
+// (kMaxRanks) | tile words (num_tiles x R)]. The accumulators sit at fixed offsets
+// sized for the largest E and N, so a workspace that is at rest stays valid for
+// any later call whatever its T, E, R; the tile words carry their epoch, so
+// stale words of earlier calls are never mistaken for current ones.
+constexpr size_t kOffExperts = 256;
+constexpr size_t kOffNodes = kOffExperts + kMaxExperts * sizeof(int32_t);
+constexpr size_t kOffWords = kOffNodes + kMaxRanks * sizeof(int32_t);
+
 extern "C" size_t ep_layout_workspace_size(int32_t T, int32_t E, int32_t R, int32_t ranks_per_node) {
+    (void)ranks_per_node;
     if (T < 0 || E <= 0 || R <= 0) return 0;
-    const int N = ranks_per_node > 0 ? R / ranks_per_node : 0;
-    return align256(sizeof(ep_layout_ws_header_t)) +
-           align256(static_cast<size_t>(num_tiles_for(T)) * R * sizeof(unsigned long long)) +
-           align256(static_cast<size_t>(E) * sizeof(int32_t)) + align256(static_cast<size_t>(N) * sizeof(int32_t));
+    return kOffWords + align256(static_cast<size_t>(num_tiles_for(T)) * R * sizeof(unsigned long long));
 }
 
 extern "C" ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E, int32_t R,
@@ -295,12 +302,9 @@ extern "C" ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t
     a.slot = slot;
     char* ws = static_cast<char*>(workspace);
     a.hdr = reinterpret_cast<ep_layout_ws_header_t*>(ws);
-    ws += align256(sizeof(ep_layout_ws_header_t));
-    a.words = reinterpret_cast<unsigned long long*>(ws);
-    ws += align256(static_cast<size_t>(a.num_tiles) * R * sizeof(unsigned long long));
-    a.acc_expert = reinterpret_cast<int32_t*>(ws);
-    ws += align256(static_cast<size_t>(E) * sizeof(int32_t));
-    a.acc_node = reinterpret_cast<int32_t*>(ws);
+    a.acc_expert = reinterpret_cast<int32_t*>(ws + kOffExperts);
+    a.acc_node = reinterpret_cast<int32_t*>(ws + kOffNodes);
+    a.words = reinterpret_cast<unsigned long long*>(ws + kOffWords);
     a.status = status;
 
     const size_t smem = static_cast<size_t>(E) * sizeof(int32_t);

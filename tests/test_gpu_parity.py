@@ -289,7 +289,44 @@ def test_layout_empty_batch_and_workspace_reuse():
         got = layout_to_host(sub)
         for key, v in got.items():
             assert np.array_equal(v, L[key]), (T, key)
+    # the same workspace, now for other E, R and node counts
+    for name, T in (("restripe", 2000), ("skewed", 1500), ("tiny", 128)):
+        w = workloads.make(name, T=T, H=8)
+        other = ep.alloc_layout(w.T, w.E, w.R, w.ranks_per_node)
+        assert lay.workspace.numel() >= ep.ep_layout_workspace_size(w.T, w.E, w.R, w.ranks_per_node)
+        other.workspace = lay.workspace
+        other.status = lay.status
+        ep.get_layout(torch.from_numpy(w.topk_idx).cuda(), w.E, w.R, w.ranks_per_node, out=other)
+        _assert_layout(w, other, oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node))
     assert ep.read_flags(lay.status) == 0
+
+
+def test_path_captured_in_a_cuda_graph():
+    """layout -> dispatch -> combine captured once in a CUDA graph and replayed: same results."""
+    w = workloads.make("dsv3", T=1000, H=1024)
+    L = oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node)
+    topk = torch.from_numpy(w.topk_idx).cuda()
+    x = dev_bf16(w.x)
+    tw = torch.from_numpy(w.topk_w).cuda()
+    M = w.max_tokens
+    lay = ep.get_layout(topk, w.E, w.R, w.ranks_per_node)
+    d = ep.dispatch(x, topk, tw, lay, M)
+    out = ep.combine(d.recv_x, lay, M)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ep.get_layout(topk, w.E, w.R, w.ranks_per_node, out=lay)
+        ep.dispatch(x, topk, tw, lay, M, out=d)
+        ep.combine(d.recv_x, lay, M, out=out)
+    for _ in range(3):
+        lay.slot.fill_(-5)
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    _assert_layout(w, lay, L)
+    D = oracle.dispatch(w.x, w.topk_idx, w.topk_w, L["slot"], w.E, w.R, M)
+    ref, _ = oracle.combine(D["recv_x"], L["slot"], M)
+    assert np.array_equal(host_bits(out), ref)
 
 
 def test_layout_bounded_wait_times_out_without_hanging():

@@ -14,9 +14,10 @@ functions here with the same names are its ctypes binding, and api.py
 allocates buffers and chains the calls.
 """
 from ._lib import (  # noqa: F401
-    ABI_VERSION, DTYPE_BF16, DTYPE_E4M3, EP_ERR_CUDA, EP_ERR_INVALID, EP_OK, EXPORTS, FLAG_BAD_EXPERT,
+    ABI_VERSION, DTYPE_BF16, DTYPE_E4M3, EP_ERR_CUDA, EP_ERR_INVALID, EP_ERR_SCRATCH, EP_OK,
+    LAYOUT_NOALLOC_SCRATCH_BYTES, EXPORTS, FLAG_BAD_EXPERT,
     FLAG_CAPACITY, FLAG_TIMEOUT, FLAG_WORKSPACE, NODES_DENSE, NODES_SPARSE, EpError, ep_combine, ep_dispatch,
-    ep_dispatch_nodes, ep_get_layout, ep_layout_workspace_size, ep_restripe_prob, lib,
+    ep_dispatch_nodes, ep_get_layout, ep_get_layout_noalloc, ep_layout_workspace_size, ep_restripe_prob, lib,
 )
 from .api import (  # noqa: F401
     Dispatched, Layout, alloc_dispatch, alloc_layout, combine, dispatch, get_layout, read_flags,

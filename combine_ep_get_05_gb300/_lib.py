@@ -19,6 +19,8 @@ from .build import LIB_PATH
 EP_OK = 0
 EP_ERR_INVALID = 1
 EP_ERR_CUDA = 2
+EP_ERR_SCRATCH = 3
+LAYOUT_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 FLAG_CAPACITY = 1
 FLAG_BAD_EXPERT = 2
@@ -35,7 +37,7 @@ ABI_VERSION = 1
 
 EXPORTS = (
     "ep_abi_version", "ep_status_str", "ep_last_cuda_error", "ep_layout_workspace_size",
-    "ep_get_layout", "ep_dispatch", "ep_restripe_prob", "ep_dispatch_nodes", "ep_combine",
+    "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_restripe_prob", "ep_dispatch_nodes", "ep_combine",
 )
 
 
@@ -73,6 +75,7 @@ def lib():
                     "ep_last_cuda_error": (i32, []),
                     "ep_layout_workspace_size": (sz, [i32, i32, i32, i32]),
                     "ep_get_layout": (i32, [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P, P]),
+                    "ep_get_layout_noalloc": (i32, [P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P]),
                     "ep_dispatch": (i32, [P, i32, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]),
                     "ep_restripe_prob": (i32, [P, i32, i32, i32, i32, P, P]),
                     "ep_dispatch_nodes": (i32, [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P, P]),
@@ -144,6 +147,27 @@ def ep_get_layout(topk_idx, num_experts, num_ranks, ranks_per_node, tokens_per_e
         _ptr(tokens_per_node) if N else None, _ptr(is_token_in_rank), _ptr(is_token_in_node) if N else None,
         _ptr(slot), _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
     _done("ep_get_layout", rc)
+
+
+def ep_get_layout_noalloc(topk_idx, num_experts, num_ranks, ranks_per_node, tokens_per_expert, tokens_per_rank,
+                          tokens_per_node, is_token_in_rank, is_token_in_node, slot, status=None, stream=None):
+    """ep_get_layout without a workspace (for callers that cannot allocate one); see include/ep.h."""
+    T, k = topk_idx.shape
+    E, R = num_experts, num_ranks
+    N = R // ranks_per_node if ranks_per_node > 0 else 0
+    _check("topk_idx", topk_idx, torch.int64)
+    _check("tokens_per_expert", tokens_per_expert, torch.int32, (E,))
+    _check("tokens_per_rank", tokens_per_rank, torch.int32, (R,))
+    _check("tokens_per_node", tokens_per_node, torch.int32, (N,), optional=N == 0)
+    _check("is_token_in_rank", is_token_in_rank, torch.uint8, (T, R))
+    _check("is_token_in_node", is_token_in_node, torch.uint8, (T, N), optional=N == 0)
+    _check("slot", slot, torch.int32, (T, R))
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_get_layout_noalloc(
+        _ptr(topk_idx), T, k, E, R, ranks_per_node, _ptr(tokens_per_expert), _ptr(tokens_per_rank),
+        _ptr(tokens_per_node) if N else None, _ptr(is_token_in_rank), _ptr(is_token_in_node) if N else None,
+        _ptr(slot), _ptr(status), _stream(stream))
+    _done("ep_get_layout_noalloc", rc)
 
 
 def ep_dispatch(x, out_dtype, topk_idx, topk_w, slot, num_experts, num_ranks, max_tokens, recv_x,

@@ -44,6 +44,9 @@ const char* ep_status_str(ep_status_t s) {
         case EP_OK: return "EP_OK";
         case EP_ERR_INVALID: return "EP_ERR_INVALID: an argument was rejected; nothing was launched";
         case EP_ERR_CUDA: return "EP_ERR_CUDA: a CUDA launch or runtime call failed";
+        case EP_ERR_SCRATCH:
+            return "EP_ERR_SCRATCH: the sizes need more layout workspace than the fixed scratch of "
+                   "ep_get_layout_noalloc holds; call ep_get_layout with a workspace instead";
         default: return "unknown ep_status_t";
     }
 }

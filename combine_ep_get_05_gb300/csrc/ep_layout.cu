@@ -24,6 +24,8 @@
 //      the last CTA to finish moves them to the outputs, zeroes the
 //      accumulators and the counters and advances the epoch, so the workspace
 //      is ready for the next call without a memset.
+#include <mutex>
+
 #include "ep_common.cuh"
 
 namespace {
@@ -317,5 +319,111 @@ extern "C" ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t
         g_smem_attr_set[dev] = true;
     }
     layout_kernel<<<a.num_tiles, kTileTokens, smem, as_stream(stream)>>>(a);
+    return check_launch();
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: ep_get_layout_noalloc
+// ---------------------------------------------------------------------------
+// Some callers cannot hand the layout a workspace: code that runs where device
+// allocation is forbidden or unavailable (a caller with a fixed, pre-planned
+// memory budget and no allocator of its own, a host runtime that only passes
+// pointers to tensors it already owns, or a plain C caller without a CUDA
+// allocator). For them the workspace lives in this fixed-size device array
+// instead. It is part of the library image: every GPU that loads the library
+// holds these bytes until the process exits. All calls on a device share it,
+// so calls whose kernels overlap on the GPU (different streams, no ordering
+// between them) race and must not be issued.
+static __device__ __align__(256) unsigned char g_layout_scratch[EP_LAYOUT_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = EP_LAYOUT_NOALLOC_SCRATCH_BYTES;
+static_assert(kNoAllocScratchBytes > kOffWords, "scratch must hold the fixed workspace part");
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};
+
+// Device address of g_layout_scratch on the current device, looked up once per
+// device (host code must not use the symbol itself: on the host it names a
+// host-side shadow, not device memory).
+ep_status_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return cuda_fail(err);
+    if (dev < 0 || dev >= 64) return EP_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_layout_scratch);
+        if (err != cudaSuccess || p == nullptr) return cuda_fail(err != cudaSuccess ? err : cudaErrorInvalidSymbol);
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return EP_OK;
+}
+
+}  // namespace
+
+extern "C" ep_status_t ep_get_layout_noalloc(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E, int32_t R,
+                                             int32_t ranks_per_node, int32_t* tokens_per_expert,
+                                             int32_t* tokens_per_rank, int32_t* tokens_per_node,
+                                             uint8_t* is_token_in_rank, uint8_t* is_token_in_node, int32_t* slot,
+                                             int32_t* status, void* stream) {
+    using namespace ep;
+    if (T < 0 || T >= (1 << 30) || k < 1 || k > kMaxTopk || R < 1 || R > kMaxRanks || E < R ||
+        E > kMaxExperts || E % R != 0 || ranks_per_node < 0 || ranks_per_node > R ||
+        (ranks_per_node > 0 && R % ranks_per_node != 0))
+        return EP_ERR_INVALID;
+    const bool nodes = ranks_per_node > 0;
+    if (tokens_per_expert == nullptr || tokens_per_rank == nullptr) return EP_ERR_INVALID;
+    if (T > 0 && (topk_idx == nullptr || is_token_in_rank == nullptr || slot == nullptr)) return EP_ERR_INVALID;
+    if (nodes && (tokens_per_node == nullptr || (T > 0 && is_token_in_node == nullptr))) return EP_ERR_INVALID;
+    if (!aligned16_or_null(topk_idx) || !aligned16(tokens_per_expert) || !aligned16(tokens_per_rank) ||
+        !aligned16_or_null(tokens_per_node) || !aligned16_or_null(is_token_in_rank) ||
+        !aligned16_or_null(is_token_in_node) || !aligned16_or_null(slot))
+        return EP_ERR_INVALID;
+    const size_t need = ep_layout_workspace_size(T, E, R, ranks_per_node);
+    if (need > kNoAllocScratchBytes) return EP_ERR_SCRATCH;
+
+    void* scratch = nullptr;
+    ep_status_t st = scratch_address(&scratch);
+    if (st != EP_OK) return st;
+    // the array keeps the previous call's contents: zero the part this call uses
+    cudaError_t err = cudaMemsetAsync(scratch, 0, need, as_stream(stream));
+    if (err != cudaSuccess) return cuda_fail(err);
+
+    LayoutArgs a{};
+    a.topk_idx = topk_idx;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.R = R;
+    a.rpn = nodes ? ranks_per_node : 1;
+    a.N = nodes ? R / ranks_per_node : 0;
+    a.epr = E / R;
+    a.num_tiles = num_tiles_for(T);
+    a.tokens_per_expert = tokens_per_expert;
+    a.tokens_per_rank = tokens_per_rank;
+    a.tokens_per_node = nodes ? tokens_per_node : nullptr;
+    a.in_rank = is_token_in_rank;
+    a.in_node = nodes ? is_token_in_node : nullptr;
+    a.slot = slot;
+    char* ws = static_cast<char*>(scratch);
+    a.hdr = reinterpret_cast<ep_layout_ws_header_t*>(ws);
+    a.acc_expert = reinterpret_cast<int32_t*>(ws + kOffExperts);
+    a.acc_node = reinterpret_cast<int32_t*>(ws + kOffNodes);
+    a.words = reinterpret_cast<unsigned long long*>(ws + kOffWords);
+    a.status = status;
+
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !g_smem_attr_set[dev]) {
+        err = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kMaxExperts * static_cast<int>(sizeof(int32_t)));
+        if (err != cudaSuccess) return cuda_fail(err);
+        g_smem_attr_set[dev] = true;
+    }
+    layout_kernel<<<a.num_tiles, kTileTokens, static_cast<size_t>(E) * sizeof(int32_t), as_stream(stream)>>>(a);
     return check_launch();
 }

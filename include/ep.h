@@ -51,6 +51,7 @@ typedef int32_t ep_status_t;
 #define EP_OK 0
 #define EP_ERR_INVALID 1
 #define EP_ERR_CUDA 2
+#define EP_ERR_SCRATCH 3 /* ep_get_layout_noalloc: the sizes need more than its fixed scratch */
 
 /* asynchronous error bits OR-ed into *status by the kernels */
 #define EP_FLAG_CAPACITY 1   /* a receive slot >= max_tokens was dropped ([PR #453] commit
@@ -126,6 +127,34 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t
                           uint8_t* is_token_in_rank, uint8_t* is_token_in_node, int32_t* slot,
                           void* workspace, size_t workspace_bytes, int32_t* status,
                           void* stream);
+
+/* ep_get_layout_noalloc -- ep_get_layout for callers that cannot allocate.
+ * The pages have no counterpart: this entry point exists for callers that have
+ * no way to provide the layout workspace -- code that must not allocate device
+ * memory where it runs (a fixed, pre-planned memory budget with no allocator of
+ * its own), or a host runtime that can only pass pointers to arrays it already
+ * owns. It computes exactly what ep_get_layout computes, with the same inputs,
+ * outputs, argument rules and flags, but takes no workspace: it uses a
+ * fixed-size array inside the library (EP_LAYOUT_NOALLOC_SCRATCH_BYTES of
+ * device memory that every GPU which loads the library keeps until the process
+ * exits). It never calls cudaMalloc, cudaFree or any allocating routine.
+ *   - The first call on a device looks up that array's device address once
+ *     (cudaGetSymbolAddress) with the device current; make that first call
+ *     before any stream capture.
+ *   - Each call zero-fills the part of the array it uses (an async memset on
+ *     `stream`), then launches the layout kernel.
+ *   - Sizes whose workspace (ep_layout_workspace_size) exceeds
+ *     EP_LAYOUT_NOALLOC_SCRATCH_BYTES are rejected with EP_ERR_SCRATCH before
+ *     anything is launched (e.g. T up to ~126k tokens at R = 256, ~1M at R = 32).
+ *   - All calls on a device share the array: calls whose work can overlap on the
+ *     GPU (different streams without ordering) race. Keep them on one stream.
+ */
+#define EP_LAYOUT_NOALLOC_SCRATCH_BYTES (1u << 20)
+ep_status_t ep_get_layout_noalloc(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E, int32_t R,
+                                  int32_t ranks_per_node, int32_t* tokens_per_expert,
+                                  int32_t* tokens_per_rank, int32_t* tokens_per_node,
+                                  uint8_t* is_token_in_rank, uint8_t* is_token_in_node, int32_t* slot,
+                                  int32_t* status, void* stream);
 
 /* ------------------------------------------------------------------------- */
 /* Rank-level dispatch                                                       */

@@ -4,13 +4,18 @@
 //
 //   out[t][h] = bf16_rn( ((0 + y[r0][s0][h]) + y[r1][s1][h]) + ... ),  r0 < r1 < ...
 //
-// One warp per token: the warp reads the token's slot row once (lanes across
-// ranks), compacts the contributing rows in ascending rank order with a ballot,
-// then for each 16-byte vector of the output (8 channels per lane) issues the
-// loads of up to 8 source rows at once and adds them into fp32 accumulators
-// strictly in that order (one IEEE addition per term, no reassociation), and
-// stores one bf16 vector rounded to nearest even. The kernel is bound by HBM
-// bandwidth: it reads one row per (token, rank) pair and writes T rows.
+// Work is split into items of (token, group of 32 output vectors): one warp
+// item covers 32 lanes x 8 channels = 256 channels of one token. Each CTA takes a
+// contiguous range of items, so every SM gets the same amount of work whatever
+// T is, and consecutive warps of a CTA share a token (its slot row stays in L1).
+// Per item the warp reads the token's slot row (lanes across ranks) and
+// compacts the contributing rows in ascending rank order with a ballot, issues
+// the loads of up to 8 source rows at once, and adds them into fp32
+// accumulators strictly in that order (one IEEE addition per term, no
+// reassociation); then it stores one bf16 vector rounded to nearest even. The
+// kernel is capped at 64 registers so four 256-thread CTAs fit on an SM, which
+// keeps enough loads in flight to saturate HBM: it reads one row per (token,
+// rank) pair and writes T rows.
 #include "ep_common.cuh"
 
 namespace {
@@ -19,6 +24,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxSrc = 256;  // = largest R: every rank may contribute
 constexpr int kBatch = 8;  // source rows loaded together
+constexpr int kMinBlocks = 4;  // CTAs per SM the register budget is sized for
 
 __device__ __forceinline__ void add8(float* acc, const uint4& v) {
     acc[0] = __fadd_rn(acc[0], ep::bf16_lo(v.x));
@@ -31,17 +37,23 @@ __device__ __forceinline__ void add8(float* acc, const uint4& v) {
     acc[7] = __fadd_rn(acc[7], ep::bf16_hi(v.w));
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
     combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ slot, int T, int H, int R,
                    int max_tokens, uint16_t* __restrict__ out, int32_t* status) {
     __shared__ long long s_src[kWarps][kMaxSrc];
     const int lane = ep::lane_id();
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int nvec = H / 8;
+    const int ngroups = (nvec + 31) / 32;
+    const long long items = static_cast<long long>(T) * ngroups;
+    const long long i0 = static_cast<long long>(blockIdx.x) * items / gridDim.x;
+    const long long i1 = static_cast<long long>(blockIdx.x + 1) * items / gridDim.x;
     const uint4* ys = reinterpret_cast<const uint4*>(y);
     uint4* os = reinterpret_cast<uint4*>(out);
 
-    for (int t = blockIdx.x * kWarps + warp; t < T; t += gridDim.x * kWarps) {
+    for (long long it = i0 + warp; it < i1; it += kWarps) {
+        const int t = static_cast<int>(it / ngroups);
+        const int v = static_cast<int>(it - static_cast<long long>(t) * ngroups) * 32 + lane;
         int ns = 0;
         bool over_any = false;
         for (int r0 = 0; r0 < R; r0 += 32) {
@@ -51,26 +63,24 @@ __global__ void __launch_bounds__(kThreads)
             over_any |= over;
             const bool ok = s >= 0 && !over;
             const uint32_t m = __ballot_sync(ep::kFullMask, ok);
-            if (ok) {
-                const int pos = ns + __popc(m & ep::lanemask_lt());
-                s_src[warp][pos] = (static_cast<long long>(r) * max_tokens + s) * nvec;
-            }
+            if (ok) s_src[warp][ns + __popc(m & ep::lanemask_lt())] = (static_cast<long long>(r) * max_tokens + s) * nvec;
             ns += __popc(m);
         }
-        if (over_any) ep::raise_flag(status, EP_FLAG_CAPACITY);
+        // one report per token: the item that starts the token's row
+        if (over_any && v == lane) ep::raise_flag(status, EP_FLAG_CAPACITY);
         __syncwarp();
 
-        for (int v = lane; v < nvec; v += 32) {
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int d0 = 0; d0 < ns; d0 += kBatch) {
-                uint4 buf[kBatch];
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int d0 = 0; d0 < ns; d0 += kBatch) {
+            uint4 buf[kBatch];
 #pragma unroll
-                for (int i = 0; i < kBatch; ++i)
-                    if (d0 + i < ns) buf[i] = ep::ld_stream_v4(ys + s_src[warp][d0 + i] + v);
+            for (int i = 0; i < kBatch; ++i)
+                if (d0 + i < ns && v < nvec) buf[i] = ep::ld_stream_v4(ys + s_src[warp][d0 + i] + v);
 #pragma unroll
-                for (int i = 0; i < kBatch; ++i)
-                    if (d0 + i < ns) add8(acc, buf[i]);
-            }
+            for (int i = 0; i < kBatch; ++i)
+                if (d0 + i < ns) add8(acc, buf[i]);
+        }
+        if (v < nvec) {
             uint4 o;
             o.x = ep::pack_bf16x2_rn(acc[0], acc[1]);
             o.y = ep::pack_bf16x2_rn(acc[2], acc[3]);
@@ -82,6 +92,8 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+int g_blocks_per_sm[64] = {};
+
 }  // namespace
 
 extern "C" ep_status_t ep_combine(const void* y, const int32_t* slot, int32_t T, int32_t H, int32_t R,
@@ -91,9 +103,19 @@ extern "C" ep_status_t ep_combine(const void* y, const int32_t* slot, int32_t T,
     if (T == 0) return EP_OK;
     if (slot == nullptr || out == nullptr || (max_tokens > 0 && y == nullptr)) return EP_ERR_INVALID;
     if (!aligned16_or_null(y) || !aligned16(slot) || !aligned16(out)) return EP_ERR_INVALID;
-    const int want = (T + kWarps - 1) / kWarps;
-    const int cap = sm_count() * 8;
-    const int grid = want < cap ? want : cap;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int per_sm = dev >= 0 && dev < 64 ? g_blocks_per_sm[dev] : 0;
+    if (per_sm == 0) {
+        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel, kThreads, 0);
+        if (err != cudaSuccess) return cuda_fail(err);
+        if (per_sm < 1) per_sm = 1;
+        if (dev >= 0 && dev < 64) g_blocks_per_sm[dev] = per_sm;
+    }
+    const long long items = static_cast<long long>(T) * ((H / 8 + 31) / 32);
+    const long long want = (items + kWarps - 1) / kWarps;
+    const long long cap = static_cast<long long>(sm_count()) * per_sm;
+    const int grid = static_cast<int>(want < cap ? want : cap);
     combine_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(static_cast<const uint16_t*>(y), slot, T, H, R,
                                                              max_tokens, static_cast<uint16_t*>(out), status);
     return check_launch();

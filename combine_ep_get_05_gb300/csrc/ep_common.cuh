@@ -76,6 +76,11 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
     return v;
 }
 
+// hint: bring the line holding p into L2 (no register result, never faults on a valid address)
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

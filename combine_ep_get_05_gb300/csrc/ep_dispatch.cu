@@ -20,7 +20,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxDest = 256;  // = largest R: a slot row may name every rank
 constexpr int kMaxTopk = 32;
-constexpr int kUnroll = 4;     // 16-byte vectors in flight per lane (bf16 path)
+constexpr int kUnroll = 8;     // 16-byte vectors in flight per lane (bf16 path)
 constexpr int kUnrollFp8 = 2;  // warp iterations (2 blocks of 128 each) in flight (FP8 path)
 
 struct DispatchArgs {

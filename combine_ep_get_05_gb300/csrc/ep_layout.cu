@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
     extern __shared__ int32_t s_hist[];  // [E]
     __shared__ uint32_t s_mask[kTileWarps][kMaxRanks];
     __shared__ int32_t s_wpref[kTileWarps][kMaxRanks];
+    __shared__ uint32_t s_nmask[kTileWarps][kMaxRanks];
     __shared__ int32_t s_tile_prefix[kMaxRanks];
     __shared__ uint32_t s_tile, s_epoch, s_stall, s_last;
 
@@ -90,6 +91,16 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
         s_tile = atomicAdd(&a.hdr->ticket, 1u);
         s_epoch = ld_relaxed_u32(&a.hdr->epoch) + 1u;
         s_stall = ld_relaxed_u32(&a.hdr->stall_tile);
+    }
+    {
+        // tiles are handed out roughly in launch order: warm L2 with this CTA's likely
+        // router rows while the ticket is on its way
+        const int tg = static_cast<int>(blockIdx.x) * kTileTokens + tid;
+        if (tg < a.T) {
+            const int64_t* row = a.topk_idx + static_cast<size_t>(tg) * a.k;
+            prefetch_l2(row);
+            prefetch_l2(row + a.k - 1);
+        }
     }
     for (int e = tid; e < a.E; e += kTileTokens) s_hist[e] = 0;
     __syncthreads();
@@ -147,6 +158,7 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
         for (int w = 0; w < kTileWarps; ++w) {
             uint32_t m = 0;
             for (int q = 0; q < a.rpn; ++q) m |= s_mask[w][n * a.rpn + q];
+            s_nmask[w][n] = m;
             c += __popc(m);
         }
         if (c != 0) atomicAdd(&a.acc_node[n], c);
@@ -205,25 +217,36 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
     }
     __syncthreads();
 
-    // 4. rows of is_token_in_rank / slot / is_token_in_node, lanes across ranks
-    const int ntok = a.T - t0 < kTileTokens ? a.T - t0 : kTileTokens;
-    for (int tl = warp; tl < ntok; tl += kTileWarps) {
-        const int w = tl >> 5;
-        const int ln = tl & 31;
-        const uint32_t below = (1u << ln) - 1u;
-        const size_t base = static_cast<size_t>(t0 + tl) * a.R;
-        for (int r = lane; r < a.R; r += 32) {
-            const uint32_t m = s_mask[w][r];
-            const bool in = (m >> ln) & 1u;
-            a.in_rank[base + r] = in ? 1 : 0;
-            a.slot[base + r] = in ? s_tile_prefix[r] + s_wpref[w][r] + __popc(m & below) : -1;
+    // 4. rows of is_token_in_rank / slot / is_token_in_node. Warp w writes the 32
+    //    tokens of its own ballot group: per rank it reads the group's mask word and
+    //    prefixes once, then emits 32 independent (in_rank, slot) pairs, lanes across
+    //    ranks so that each store instruction covers consecutive ranks of one token.
+    {
+        const int g0 = warp * 32;  // first tile-local token of this warp's group
+        const int ng = a.T - t0 - g0 < 32 ? a.T - t0 - g0 : 32;
+        for (int r = lane; r < a.R && ng > 0; r += 32) {
+            const uint32_t m = s_mask[warp][r];
+            const int32_t base_slot = s_tile_prefix[r] + s_wpref[warp][r];
+            uint8_t* ir = a.in_rank + static_cast<size_t>(t0 + g0) * a.R + r;
+            int32_t* sl = a.slot + static_cast<size_t>(t0 + g0) * a.R + r;
+            int before = 0;  // group tokens before u that go to rank r
+#pragma unroll 8
+            for (int u = 0; u < 32; ++u) {
+                if (u < ng) {
+                    const bool in = (m >> u) & 1u;
+                    ir[static_cast<size_t>(u) * a.R] = in ? 1 : 0;
+                    sl[static_cast<size_t>(u) * a.R] = in ? base_slot + before : -1;
+                    before += in ? 1 : 0;
+                }
+            }
         }
         if (a.in_node != nullptr) {
-            const size_t nbase = static_cast<size_t>(t0 + tl) * a.N;
-            for (int n = lane; n < a.N; n += 32) {
-                uint32_t m = 0;
-                for (int q = 0; q < a.rpn; ++q) m |= s_mask[w][n * a.rpn + q];
-                a.in_node[nbase + n] = (m >> ln) & 1u;
+            for (int n = lane; n < a.N && ng > 0; n += 32) {
+                const uint32_t m = s_nmask[warp][n];
+                uint8_t* in = a.in_node + static_cast<size_t>(t0 + g0) * a.N + n;
+#pragma unroll 8
+                for (int u = 0; u < 32; ++u)
+                    if (u < ng) in[static_cast<size_t>(u) * a.N] = (m >> u) & 1u;
             }
         }
     }

@@ -19,7 +19,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;  // 16-byte vectors in flight per lane
 constexpr int kMaxNodes = 256;
 
 struct NodeArgs {

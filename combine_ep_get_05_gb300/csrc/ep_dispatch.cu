@@ -7,8 +7,9 @@
 // Design: a persistent grid of warps, one token per warp at a time. The warp
 // reads the token's slot row once (lanes across ranks) and compacts the
 // destinations (ascending rank) into shared memory with a ballot; then it
-// streams the hidden row through registers in 16-byte vectors, reading each
-// vector once from HBM and storing it to every destination slab. Metadata
+// streams the hidden row through registers in 16-byte vectors, 8 per lane
+// (4 KB per warp) in flight, reading each vector once from HBM and storing it
+// to every destination slab. Metadata
 // (source index, local expert ids, weights) is written by one lane per
 // destination. Nothing here is a contraction, so no tensor cores: the kernel
 // is bound by HBM bandwidth (read T rows, write one row per (token, rank)).
@@ -21,7 +22,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxDest = 256;  // = largest R: a slot row may name every rank
 constexpr int kMaxTopk = 32;
 constexpr int kUnroll = 8;     // 16-byte vectors in flight per lane (bf16 path)
-constexpr int kUnrollFp8 = 2;  // warp iterations (2 blocks of 128 each) in flight (FP8 path)
+constexpr int kUnrollFp8 = 2;  // warp iterations (4 blocks of 128 each) in flight (FP8 path)
 
 struct DispatchArgs {
     const uint16_t* x;
@@ -118,72 +119,99 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(DispatchArgs a)
     }
 }
 
-// One 128-element block held by a half warp: 8 bf16 per lane.
-// Returns the 8 E4M3 codes (lo word: elements 0..3, hi word: 4..7) and the scale.
-__device__ __forceinline__ void quantize8(const uint4& v, uint32_t& q_lo, uint32_t& q_hi, float& scale) {
-    float f[8];
-    f[0] = ep::bf16_lo(v.x); f[1] = ep::bf16_hi(v.x);
-    f[2] = ep::bf16_lo(v.y); f[3] = ep::bf16_hi(v.y);
-    f[4] = ep::bf16_lo(v.z); f[5] = ep::bf16_hi(v.z);
-    f[6] = ep::bf16_lo(v.w); f[7] = ep::bf16_hi(v.w);
+// One 128-element block is held by 8 lanes, 16 bf16 (two 16-byte vectors) per
+// lane. Returns the lane's 16 E4M3 codes as one 16-byte vector (element i in
+// byte i) and the block's scale (the same in all 8 lanes).
+__device__ __forceinline__ void quantize16(const uint4& a, const uint4& b, uint4& q, float& scale) {
+    float f[16];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = ep::bf16_lo(w[i]);
+        f[2 * i + 1] = ep::bf16_hi(w[i]);
+    }
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    // max over the 16 lanes of this half warp (xor offsets < 16 stay in the half)
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    // max over the 8 lanes of this block (xor offsets < 8 stay in the group)
 #pragma unroll
-    for (int off = 8; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(ep::kFullMask, amax, off));
+    for (int off = 4; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(ep::kFullMask, amax, off));
     scale = __fdiv_rn(amax, 448.0f);
-    uint32_t c[4];
+    uint32_t c[8];
     if (amax == 0.0f) {
         // all elements are +-0: keep the sign of each zero
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i)
             c[i] = ((__float_as_uint(f[2 * i]) >> 31) ? 0x80u : 0u) |
                    ((__float_as_uint(f[2 * i + 1]) >> 31) ? 0x8000u : 0u);
     } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i)
             c[i] = ep::pack_e4m3x2_rn_sat(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
     }
-    q_lo = c[0] | (c[1] << 16);
-    q_hi = c[2] | (c[3] << 16);
+    q.x = c[0] | (c[1] << 16);
+    q.y = c[2] | (c[3] << 16);
+    q.z = c[4] | (c[5] << 16);
+    q.w = c[6] | (c[7] << 16);
 }
 
+// FP8 dispatch: a warp iteration covers 4 blocks (512 elements); lane l owns
+// elements 16*(l % 8) .. +15 of block l / 8, so every code store is one 16-byte
+// vector per lane (512 bytes per warp instruction) and the 4 scales of an
+// iteration leave in one 16-byte store when they are 16-byte aligned.
 __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a) {
     __shared__ int s_rank[kWarps][kMaxDest];
     __shared__ long long s_row[kWarps][kMaxDest];
     const int lane = ep::lane_id();
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int nblk = a.H / 128;
-    const int half = lane >> 4;   // which of the two blocks of a warp iteration
-    const int hl = lane & 15;     // 16-byte vector within the block
+    const int grp = lane >> 3;  // block of the iteration this lane works on (0..3)
+    const int pos = lane & 7;   // 16-element slice within the block
+    const bool vec_scales = (nblk & 3) == 0;
     uint8_t* recv = static_cast<uint8_t*>(a.recv_x);
 
     for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
         const int nd = gather_destinations(a, t, s_rank[warp], s_row[warp]);
         write_metadata(a, t, nd, s_rank[warp], s_row[warp]);
         const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H);
-        for (int b0 = 0; b0 < nblk; b0 += 2 * kUnrollFp8) {
-            uint4 in[kUnrollFp8];
+        for (int b0 = 0; b0 < nblk; b0 += 4 * kUnrollFp8) {
+            uint4 lo[kUnrollFp8], hi[kUnrollFp8];
 #pragma unroll
             for (int u = 0; u < kUnrollFp8; ++u) {
-                const int b = b0 + 2 * u + half;
-                in[u] = b < nblk ? ep::ld_stream_v4(src + b * 16 + hl) : make_uint4(0, 0, 0, 0);
+                const int b = b0 + 4 * u + grp;
+                if (b < nblk) {
+                    lo[u] = ep::ld_stream_v4(src + b * 16 + 2 * pos);
+                    hi[u] = ep::ld_stream_v4(src + b * 16 + 2 * pos + 1);
+                } else {
+                    lo[u] = make_uint4(0, 0, 0, 0);
+                    hi[u] = lo[u];
+                }
             }
-            uint32_t qlo[kUnrollFp8], qhi[kUnrollFp8];
+            uint4 q[kUnrollFp8];
             float sc[kUnrollFp8];
+            float4 sc4[kUnrollFp8];
 #pragma unroll
-            for (int u = 0; u < kUnrollFp8; ++u) quantize8(in[u], qlo[u], qhi[u], sc[u]);
+            for (int u = 0; u < kUnrollFp8; ++u) {
+                quantize16(lo[u], hi[u], q[u], sc[u]);
+                sc4[u].x = __shfl_sync(ep::kFullMask, sc[u], 0);
+                sc4[u].y = __shfl_sync(ep::kFullMask, sc[u], 8);
+                sc4[u].z = __shfl_sync(ep::kFullMask, sc[u], 16);
+                sc4[u].w = __shfl_sync(ep::kFullMask, sc[u], 24);
+            }
             for (int d = 0; d < nd; ++d) {
                 const size_t row = static_cast<size_t>(s_row[warp][d]);
                 uint8_t* dst = recv + row * a.H;
                 float* dsc = a.recv_scales + row * nblk;
 #pragma unroll
                 for (int u = 0; u < kUnrollFp8; ++u) {
-                    const int b = b0 + 2 * u + half;
-                    if (b < nblk) {
-                        ep::st_v2(dst + b * 128 + hl * 8, qlo[u], qhi[u]);
-                        if (hl == 0) dsc[b] = sc[u];
+                    const int b = b0 + 4 * u + grp;
+                    if (b < nblk) ep::st_v4(dst + b * 128 + pos * 16, q[u]);
+                    if (vec_scales) {
+                        if (lane == 0 && b0 + 4 * u < nblk) ep::st_v4(dsc + b0 + 4 * u, make_uint4(
+                            __float_as_uint(sc4[u].x), __float_as_uint(sc4[u].y), __float_as_uint(sc4[u].z),
+                            __float_as_uint(sc4[u].w)));
+                    } else if (pos == 0 && b < nblk) {
+                        dsc[b] = sc[u];
                     }
                 }
             }

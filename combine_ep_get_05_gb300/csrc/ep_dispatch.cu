@@ -22,6 +22,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxDest = 256;  // = largest R: a slot row may name every rank
 constexpr int kMaxTopk = 32;
 constexpr int kUnroll = 8;     // 16-byte vectors in flight per lane (bf16 path)
+constexpr int kRegDest = 8;    // destinations whose row offsets a warp keeps in registers
 constexpr int kUnrollFp8 = 2;  // warp iterations (4 blocks of 128 each) in flight (FP8 path)
 
 struct DispatchArgs {
@@ -87,7 +88,7 @@ __device__ __forceinline__ void write_metadata(const DispatchArgs& a, int t, int
     }
 }
 
-__global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(DispatchArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) dispatch_bf16_kernel(DispatchArgs a) {
     __shared__ int s_rank[kWarps][kMaxDest];
     __shared__ long long s_row[kWarps][kMaxDest];
     const int lane = ep::lane_id();
@@ -99,6 +100,10 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(DispatchArgs a)
         const int nd = gather_destinations(a, t, s_rank[warp], s_row[warp]);
         write_metadata(a, t, nd, s_rank[warp], s_row[warp]);
         const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H);
+        // the first kRegDest destination rows stay in registers for the whole row
+        uint32_t row_of[kRegDest];  // R * max_tokens < 2^31 is checked on the host
+#pragma unroll
+        for (int d = 0; d < kRegDest; ++d) row_of[d] = d < nd ? static_cast<uint32_t>(s_row[warp][d]) : 0u;
         for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
             uint4 buf[kUnroll];
 #pragma unroll
@@ -106,7 +111,18 @@ __global__ void __launch_bounds__(kThreads) dispatch_bf16_kernel(DispatchArgs a)
                 const int v = v0 + u * 32 + lane;
                 if (v < nvec) buf[u] = ep::ld_stream_v4(src + v);
             }
-            for (int d = 0; d < nd; ++d) {
+#pragma unroll
+            for (int d = 0; d < kRegDest; ++d) {
+                if (d < nd) {
+                    uint4* dst = recv + static_cast<size_t>(row_of[d]) * nvec;
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u) {
+                        const int v = v0 + u * 32 + lane;
+                        if (v < nvec) ep::st_v4(dst + v, buf[u]);
+                    }
+                }
+            }
+            for (int d = kRegDest; d < nd; ++d) {
                 uint4* dst = recv + static_cast<size_t>(s_row[warp][d]) * nvec;
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
@@ -239,6 +255,7 @@ extern "C" ep_status_t ep_dispatch(const void* x, ep_dtype_t out_dtype, const in
     if (T < 0 || H <= 0 || H % 8 != 0 || (fp8 && H % 128 != 0) || k < 1 || k > kMaxTopk || R < 1 ||
         R > 256 || E < R || E % R != 0 || max_tokens < 0)
         return EP_ERR_INVALID;
+    if (static_cast<long long>(R) * max_tokens > 0x7fffffffLL) return EP_ERR_INVALID;
     if (recv_x == nullptr || (fp8 && recv_scales == nullptr) || (!fp8 && recv_scales != nullptr))
         return EP_ERR_INVALID;
     if (T > 0 && (x == nullptr || topk_idx == nullptr || slot == nullptr)) return EP_ERR_INVALID;

@@ -10,8 +10,8 @@
 // One launch, one tile of 256 tokens per CTA (thread = token):
 //   1. each thread reads its token's k expert ids, bumps a shared-memory expert
 //      histogram and forms its rank bit mask (R <= 256: four 64-bit words);
-//   2. per rank, one warp ballot gives the 32-token membership mask of each
-//      warp; popcounts give per-warp counts and in-warp prefixes;
+//   2. a warp-level bit-matrix transpose gives, per rank, the 32-token membership
+//      mask of each warp; popcounts give per-warp counts and in-warp prefixes;
 //   3. the tile's per-rank counts are scanned across tiles with a decoupled
 //      look-back: every (tile, rank) publishes one 64-bit word holding
 //      {epoch, state, count}; state 1 = this tile's count only, state 2 = the
@@ -71,8 +71,19 @@ __device__ __forceinline__ uint32_t word_epoch(unsigned long long w) { return st
 __device__ __forceinline__ uint32_t word_state(unsigned long long w) { return static_cast<uint32_t>(w >> 30) & 3u; }
 __device__ __forceinline__ uint32_t word_value(unsigned long long w) { return static_cast<uint32_t>(w) & 0x3fffffffu; }
 
-__device__ __forceinline__ uint64_t pick_word(uint64_t m0, uint64_t m1, uint64_t m2, uint64_t m3, int r) {
-    return r < 64 ? m0 : (r < 128 ? m1 : (r < 192 ? m2 : m3));
+// Transpose of a 32 x 32 bit matrix held one row per lane (bit j of lane i =
+// A[i][j]): returns column `lane`, i.e. bit i of the result = A[i][lane]. Five
+// levels swap the off-diagonal blocks of size 16, 8, 4, 2, 1 between lane pairs.
+__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
+    const uint32_t low_cols[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int level = 0; level < 5; ++level) {
+        const int s = 16 >> level;
+        const uint32_t m = low_cols[level];
+        const uint32_t y = __shfl_xor_sync(kFullMask, x, s);
+        x = (lane & s) ? ((x & ~m) | ((y >> s) & m)) : ((x & m) | ((y & m) << s));
+    }
+    return x;
 }
 
 __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
@@ -140,11 +151,13 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
         if (bad) raise_flag(a.status, EP_FLAG_BAD_EXPERT);
     }
 
-    // 2. per-rank warp membership masks
-    for (int r = 0; r < a.R; ++r) {
-        const uint32_t bit = static_cast<uint32_t>(pick_word(m0, m1, m2, m3, r) >> (r & 63)) & 1u;
-        const uint32_t m = __ballot_sync(kFullMask, bit);
-        if (lane == (r & 31)) s_mask[warp][r] = m;
+    // 2. per-rank warp membership masks: for each chunk of 32 ranks, the warp holds a
+    //    32 x 32 bit matrix (lane = token, bit = rank); transposing it leaves in lane j
+    //    the 32-token mask of rank 32c + j (what a ballot per rank would give).
+    for (int c = 0; c * 32 < a.R; ++c) {
+        const uint64_t word = c < 2 ? m0 : (c < 4 ? m1 : (c < 6 ? m2 : m3));
+        const uint32_t m = transpose32(static_cast<uint32_t>(word >> ((c & 1) * 32)), lane);
+        if (c * 32 + lane < a.R) s_mask[warp][c * 32 + lane] = m;
     }
     __syncthreads();
 

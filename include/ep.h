@@ -180,7 +180,7 @@ ep_status_t ep_get_layout_noalloc(const int64_t* topk_idx, int32_t T, int32_t k,
  *   topk_idx      int64 [T][k], topk_w fp32 [T][k] (topk_w may be NULL when
  *                 recv_topk_w is NULL)
  *   slot          int32 [T][R] from ep_get_layout
- *   recv_x        [R][max_tokens][H] of out_dtype           (required)
+ *   recv_x        [R][max_tokens][H] of out_dtype (required); R * max_tokens < 2^31
  *   recv_scales   fp32 [R][max_tokens][H/128]               (E4M3 only, else NULL)
  *   recv_src_idx  int32 [R][max_tokens]                     (nullable)
  *   recv_topk_idx int32 [R][max_tokens][k]                  (nullable)

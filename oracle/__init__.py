@@ -73,6 +73,10 @@ def _load():
                 "oracle_dispatch_nodes": (i32, [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P]),
                 "oracle_combine": (i32, [P, P, i32, i32, i32, i32, P]),
                 "oracle_expert_scale": (None, [P, i32, P, P, P, i32, i32, i32, i32, P]),
+                "oracle_expert_layout": (i32, [P, i32, i32, i32, P, P]),
+                "oracle_dispatch_permuted": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]),
+                "oracle_permute_received": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P]),
+                "oracle_combine_permuted": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -229,3 +233,66 @@ def expert_scale(recv_x, recv_topk_w, tokens_per_rank, recv_scales=None, fill: i
     _load().oracle_expert_scale(_ptr(rx), 1 if fp8 else 0, _ptr(sc), _ptr(tw), _ptr(tpr), R,
                                 max_tokens, H, k, _ptr(y))
     return y
+
+
+# --------------------------------------------------------------------------- expert-major
+
+def expert_layout(topk_idx, E: int) -> dict:
+    ti = _c(topk_idx, np.int64)
+    T, k = ti.shape
+    out = {"expert_offsets": np.zeros(E + 1, np.int32), "expert_slot": np.zeros((T, k), np.int32)}
+    out["flags"] = int(_load().oracle_expert_layout(_ptr(ti), T, k, E, _ptr(out["expert_offsets"]),
+                                                   _ptr(out["expert_slot"])))
+    return out
+
+
+def rows_per_rank(expert_offsets, E: int, R: int) -> np.ndarray:
+    """Entries each rank's expert-major slab holds (plain indexing of the offsets)."""
+    epr = E // R
+    off = np.asarray(expert_offsets)
+    return (off[np.arange(1, R + 1) * epr] - off[np.arange(R) * epr]).astype(np.int32)
+
+
+def dispatch_permuted(x_bits, topk_idx, topk_w, EL: dict, E: int, R: int, max_rows: int, fill_x: int = 0,
+                      fill_idx: int = 0, fill_w: float = 0.0) -> dict:
+    x = _c(x_bits, np.uint16)
+    ti = _c(topk_idx, np.int64)
+    tw = _c(topk_w, np.float32)
+    T, H = x.shape
+    k = ti.shape[1]
+    out = {"perm_x": np.full((R, max_rows, H), fill_x, np.uint16),
+           "perm_src": np.full((R, max_rows), fill_idx, np.int32),
+           "perm_w": np.full((R, max_rows), fill_w, np.float32)}
+    out["flags"] = int(_load().oracle_dispatch_permuted(
+        _ptr(x), _ptr(ti), _ptr(tw), _ptr(_c(EL["expert_offsets"], np.int32)), _ptr(_c(EL["expert_slot"], np.int32)),
+        T, H, k, E, R, max_rows, _ptr(out["perm_x"]), _ptr(out["perm_src"]), _ptr(out["perm_w"])))
+    return out
+
+
+def permute_received(D: dict, tokens_per_rank, EL: dict, T: int, E: int, R: int, max_rows: int, fill_x: int = 0,
+                     fill_idx: int = 0, fill_w: float = 0.0) -> dict:
+    rx = _c(D["recv_x"], np.uint16)
+    R_, M, H = rx.shape
+    k = D["recv_topk_idx"].shape[2]
+    out = {"perm_x": np.full((R, max_rows, H), fill_x, np.uint16),
+           "perm_src": np.full((R, max_rows), fill_idx, np.int32),
+           "perm_w": np.full((R, max_rows), fill_w, np.float32)}
+    out["flags"] = int(_load().oracle_permute_received(
+        _ptr(rx), _ptr(_c(D["recv_src_idx"], np.int32)), _ptr(_c(D["recv_topk_idx"], np.int32)),
+        _ptr(_c(D["recv_topk_w"], np.float32)), _ptr(_c(tokens_per_rank, np.int32)),
+        _ptr(_c(EL["expert_offsets"], np.int32)), _ptr(_c(EL["expert_slot"], np.int32)), T, H, k, E, R, M,
+        max_rows, _ptr(out["perm_x"]), _ptr(out["perm_src"]), _ptr(out["perm_w"])))
+    return out
+
+
+def combine_permuted(y_bits, topk_idx, topk_w, EL: dict, E: int, R: int) -> tuple:
+    y = _c(y_bits, np.uint16)
+    ti = _c(topk_idx, np.int64)
+    tw = None if topk_w is None else _c(topk_w, np.float32)
+    _, max_rows, H = y.shape
+    T, k = ti.shape
+    out = np.zeros((T, H), np.uint16)
+    flags = int(_load().oracle_combine_permuted(
+        _ptr(y), _ptr(ti), _ptr(tw), _ptr(_c(EL["expert_offsets"], np.int32)), _ptr(_c(EL["expert_slot"], np.int32)),
+        T, H, k, E, R, max_rows, _ptr(out)))
+    return out, flags

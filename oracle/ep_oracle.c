@@ -384,6 +384,166 @@ int32_t oracle_combine(const uint16_t* y, const int32_t* slot, int32_t T, int32_
 }
 
 /* ------------------------------------------------------------------------- */
+/* Expert-major layout, permuted dispatch, receive-side permute, combine       */
+/* ------------------------------------------------------------------------- */
+
+/* [PR #634] "Hybrid ep nixl restripe", commit "hybrid_ep: fix scan permute-fusion
+ * local-experts sum array sizing" and the "dispatch+permute" rows of its B300 results:
+ * after dispatch the tokens a rank receives are permuted into local-expert order, from a
+ * scan over tokens and a per-local-expert sum array. Written out:
+ *   count[e]          = number of (t, j) whose expert is e (each token's ids distinct)
+ *   expert_offsets[e] = sum of count[e'] for e' < e   (expert_offsets[E] = total)
+ *   expert_slot[t][j] = number of (t', j') before (t, j), in token-then-slot order,
+ *                       with the same expert; -1 for an empty slot (< 0), an id >= E, or a
+ *                       repeat of an id earlier in the same row (the last two raise
+ *                       ORACLE_FLAG_BAD_EXPERT).
+ * Experts of a rank are contiguous, so expert order is rank-major: rank r's entries are
+ * expert_offsets[r*(E/R)] .. expert_offsets[(r+1)*(E/R)], grouped by local expert. */
+int32_t oracle_expert_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E,
+                             int32_t* expert_offsets, int32_t* expert_slot) {
+    int32_t flags = 0;
+    int32_t* cnt = (int32_t*)calloc((size_t)E + 1, sizeof(int32_t));
+    for (int32_t t = 0; t < T; ++t) {
+        for (int32_t j = 0; j < k; ++j) {
+            int64_t e = topk_idx[(size_t)t * k + j];
+            int32_t out = -1;
+            if (e >= E) {
+                flags |= ORACLE_FLAG_BAD_EXPERT;
+            } else if (e >= 0) {
+                int repeat = 0;
+                for (int32_t jj = 0; jj < j; ++jj)
+                    if (topk_idx[(size_t)t * k + jj] == e) repeat = 1;
+                if (repeat) {
+                    flags |= ORACLE_FLAG_BAD_EXPERT;
+                } else {
+                    out = cnt[e];
+                    cnt[e] += 1;
+                }
+            }
+            expert_slot[(size_t)t * k + j] = out;
+        }
+    }
+    expert_offsets[0] = 0;
+    for (int32_t e = 0; e < E; ++e) expert_offsets[e + 1] = expert_offsets[e] + cnt[e];
+    free(cnt);
+    return flags;
+}
+
+/* row of (t, j) inside its rank's expert-major slab */
+static int32_t permuted_row(const int32_t* expert_offsets, const int32_t* expert_slot, int32_t t,
+                            int32_t j, int32_t k, int64_t e, int32_t E, int32_t R) {
+    int32_t epr = E / R;
+    int32_t r = (int32_t)(e / epr);
+    return expert_offsets[e] - expert_offsets[r * epr] + expert_slot[(size_t)t * k + j];
+}
+
+/* Dispatch and permute fused: for every (t, j) with expert_slot[t][j] >= 0, expert e on
+ * rank r = e / (E/R), and p = expert_offsets[e] - expert_offsets[r*(E/R)] + expert_slot:
+ *   perm_x[r][p] = x[t], perm_src[r][p] = t, perm_w[r][p] = topk_w[t][j].
+ * A token with two experts on one rank occupies two rows. p >= max_rows is dropped and
+ * raises ORACLE_FLAG_CAPACITY. Other rows are not written. */
+int32_t oracle_dispatch_permuted(const uint16_t* x, const int64_t* topk_idx, const float* topk_w,
+                                 const int32_t* expert_offsets, const int32_t* expert_slot,
+                                 int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
+                                 int32_t max_rows, uint16_t* perm_x, int32_t* perm_src,
+                                 float* perm_w) {
+    int32_t flags = 0;
+    for (int32_t t = 0; t < T; ++t) {
+        for (int32_t j = 0; j < k; ++j) {
+            if (expert_slot[(size_t)t * k + j] < 0) continue;
+            int64_t e = topk_idx[(size_t)t * k + j];
+            int32_t r = (int32_t)(e / (E / R));
+            int32_t p = permuted_row(expert_offsets, expert_slot, t, j, k, e, E, R);
+            if (p >= max_rows) {
+                flags |= ORACLE_FLAG_CAPACITY;
+                continue;
+            }
+            size_t row = (size_t)r * max_rows + (size_t)p;
+            for (int32_t h = 0; h < H; ++h) perm_x[row * H + h] = x[(size_t)t * H + h];
+            if (perm_src != NULL) perm_src[row] = t;
+            if (perm_w != NULL) perm_w[row] = topk_w[(size_t)t * k + j];
+        }
+    }
+    return flags;
+}
+
+/* The receive phase of a split (hook-mode) dispatch ([PR #347] 2.1: the send phase
+ * returns first, the receive phase runs later): every row s < min(tokens_per_rank[r],
+ * max_tokens) that rank r received from a rank-level dispatch, for every slot j whose
+ * local expert id l = recv_topk_idx[r][s][j] >= 0, goes to the same expert-major row the
+ * fused dispatch uses (t = recv_src_idx[r][s], e = r*(E/R) + l):
+ *   perm_x[r][p] = recv_x[r][s], perm_src[r][p] = t, perm_w[r][p] = recv_topk_w[r][s][j]. */
+int32_t oracle_permute_received(const uint16_t* recv_x, const int32_t* recv_src_idx,
+                                const int32_t* recv_topk_idx, const float* recv_topk_w,
+                                const int32_t* tokens_per_rank, const int32_t* expert_offsets,
+                                const int32_t* expert_slot, int32_t T, int32_t H, int32_t k,
+                                int32_t E, int32_t R, int32_t max_tokens, int32_t max_rows,
+                                uint16_t* perm_x, int32_t* perm_src, float* perm_w) {
+    int32_t flags = 0;
+    int32_t epr = E / R;
+    (void)T;
+    for (int32_t r = 0; r < R; ++r) {
+        int32_t n = tokens_per_rank[r] < max_tokens ? tokens_per_rank[r] : max_tokens;
+        for (int32_t s = 0; s < n; ++s) {
+            size_t in_row = (size_t)r * max_tokens + s;
+            int32_t t = recv_src_idx[in_row];
+            for (int32_t j = 0; j < k; ++j) {
+                int32_t l = recv_topk_idx[in_row * k + j];
+                if (l < 0 || expert_slot[(size_t)t * k + j] < 0) continue;
+                int32_t e = r * epr + l;
+                int32_t p = expert_offsets[e] - expert_offsets[r * epr] + expert_slot[(size_t)t * k + j];
+                if (p >= max_rows) {
+                    flags |= ORACLE_FLAG_CAPACITY;
+                    continue;
+                }
+                size_t row = (size_t)r * max_rows + (size_t)p;
+                for (int32_t h = 0; h < H; ++h) perm_x[row * H + h] = recv_x[in_row * H + h];
+                if (perm_src != NULL) perm_src[row] = t;
+                if (perm_w != NULL) perm_w[row] = recv_topk_w[in_row * k + j];
+            }
+        }
+    }
+    return flags;
+}
+
+/* Combine from the expert-major slabs:
+ *   acc = 0 (fp32); for j = 0, 1, ..., k-1 with expert_slot[t][j] >= 0:
+ *       term = float(y[r][p][h]), times topk_w[t][j] (one fp32 multiply) when weighted
+ *       acc  = acc + term
+ *   out[t][h] = bf16_rn(acc)
+ * Reading: the token's own top-k order fixes the order of the terms; rows p >= max_rows
+ * were never written and are skipped with ORACLE_FLAG_CAPACITY. */
+int32_t oracle_combine_permuted(const uint16_t* y, const int64_t* topk_idx, const float* topk_w,
+                                const int32_t* expert_offsets, const int32_t* expert_slot,
+                                int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
+                                int32_t max_rows, uint16_t* out) {
+    int32_t flags = 0;
+    float* acc = (float*)malloc((size_t)H * sizeof(float) + 1);
+    for (int32_t t = 0; t < T; ++t) {
+        for (int32_t h = 0; h < H; ++h) acc[h] = 0.0f;
+        for (int32_t j = 0; j < k; ++j) {
+            if (expert_slot[(size_t)t * k + j] < 0) continue;
+            int64_t e = topk_idx[(size_t)t * k + j];
+            int32_t r = (int32_t)(e / (E / R));
+            int32_t p = permuted_row(expert_offsets, expert_slot, t, j, k, e, E, R);
+            if (p >= max_rows) {
+                flags |= ORACLE_FLAG_CAPACITY;
+                continue;
+            }
+            const uint16_t* row = y + ((size_t)r * max_rows + p) * H;
+            for (int32_t h = 0; h < H; ++h) {
+                float term = oracle_bf16_to_f32(row[h]);
+                if (topk_w != NULL) term = term * topk_w[(size_t)t * k + j];
+                acc[h] = acc[h] + term;
+            }
+        }
+        for (int32_t h = 0; h < H; ++h) out[(size_t)t * H + h] = oracle_f32_to_bf16(acc[h]);
+    }
+    free(acc);
+    return flags;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Harness expert (between dispatch and combine; not a step of the path)      */
 /* ------------------------------------------------------------------------- */
 

@@ -66,6 +66,35 @@ int32_t oracle_dispatch_nodes(const uint16_t* x, const float* prob_staging,
 int32_t oracle_combine(const uint16_t* y, const int32_t* slot, int32_t T, int32_t H, int32_t R,
                        int32_t max_tokens, uint16_t* out);
 
+/* expert-major layout: offsets [E+1] (exclusive sums of the per-expert counts, in
+ * expert order) and expert_slot [T][k] = the stable position of (t, j) among the
+ * entries of its expert, or -1. A repeated id in one token's row keeps only its
+ * first occurrence (the repeat gets -1 and raises ORACLE_FLAG_BAD_EXPERT). */
+int32_t oracle_expert_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E,
+                             int32_t* expert_offsets, int32_t* expert_slot);
+
+/* fused dispatch + permute into expert-major rank slabs [R][max_rows][H] */
+int32_t oracle_dispatch_permuted(const uint16_t* x, const int64_t* topk_idx, const float* topk_w,
+                                 const int32_t* expert_offsets, const int32_t* expert_slot,
+                                 int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
+                                 int32_t max_rows, uint16_t* perm_x, int32_t* perm_src,
+                                 float* perm_w);
+
+/* receive-side permute of rank-level dispatch output into the same expert-major slabs */
+int32_t oracle_permute_received(const uint16_t* recv_x, const int32_t* recv_src_idx,
+                                const int32_t* recv_topk_idx, const float* recv_topk_w,
+                                const int32_t* tokens_per_rank, const int32_t* expert_offsets,
+                                const int32_t* expert_slot, int32_t T, int32_t H, int32_t k,
+                                int32_t E, int32_t R, int32_t max_tokens, int32_t max_rows,
+                                uint16_t* perm_x, int32_t* perm_src, float* perm_w);
+
+/* combine from expert-major slabs: out[t] = bf16(sum over j ascending of w_j * y), weighted
+ * when topk_w is not NULL (one fp32 multiply and one fp32 add per term), plain sum otherwise */
+int32_t oracle_combine_permuted(const uint16_t* y, const int64_t* topk_idx, const float* topk_w,
+                                const int32_t* expert_offsets, const int32_t* expert_slot,
+                                int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
+                                int32_t max_rows, uint16_t* out);
+
 /* the test harness's stand-in expert (not part of the path): every received row
  * scaled by the sum, in j order, of its top-k weights on that rank */
 void oracle_expert_scale(const void* recv_x, int32_t in_fp8, const float* recv_scales,

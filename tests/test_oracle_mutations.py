@@ -14,6 +14,7 @@ import oracle
 import test_oracle_formats as F
 import test_oracle_pages as G
 import test_oracle_path as PTH
+import test_oracle_permuted as PERM
 
 MUTATIONS = [
     ("bf16 ties away from even",
@@ -72,6 +73,26 @@ MUTATIONS = [
      "for (int32_t h = 0; h < H; ++h) acc[h] = acc[h] + oracle_bf16_to_f32(row[h]);",
      "for (int32_t h = 0; h < H; ++h) acc[h] = oracle_bf16_to_f32(oracle_f32_to_bf16(acc[h] + oracle_bf16_to_f32(row[h])));",
      [PTH.test_combine_sums_in_ascending_rank_order]),
+    ("expert slot counts from 1",
+     "out = cnt[e];",
+     "out = cnt[e] + 1;",
+     [PERM.test_expert_layout_matches_stable_sort_restatement]),
+    ("expert layout keeps repeated ids",
+     "if (topk_idx[(size_t)t * k + jj] == e) repeat = 1;",
+     "if (0) repeat = 1;",
+     [PERM.test_expert_layout_repeats_and_out_of_range_are_dropped_and_flagged]),
+    ("permuted row ignores the rank's first expert offset",
+     "return expert_offsets[e] - expert_offsets[r * epr] + expert_slot[(size_t)t * k + j];",
+     "return expert_offsets[e] - expert_offsets[0 * epr + r * 0] + expert_slot[(size_t)t * k + j];",
+     [PERM.test_dispatch_permuted_groups_rows_by_local_expert_in_token_order]),
+    ("weighted combine drops the weight",
+     "if (topk_w != NULL) term = term * topk_w[(size_t)t * k + j];",
+     "if (topk_w != NULL) term = term * 1.0f;",
+     [PERM.test_combine_permuted_closed_form_and_brute_force]),
+    ("combine from expert slabs sums slots in reverse",
+     "        for (int32_t j = 0; j < k; ++j) {\n            if (expert_slot[(size_t)t * k + j] < 0) continue;\n            int64_t e = topk_idx[(size_t)t * k + j];\n            int32_t r = (int32_t)(e / (E / R));\n            int32_t p = permuted_row(expert_offsets, expert_slot, t, j, k, e, E, R);\n            if (p >= max_rows) {\n                flags |= ORACLE_FLAG_CAPACITY;\n                continue;\n            }\n            const uint16_t* row",
+     "        for (int32_t j = k - 1; j >= 0; --j) {\n            if (expert_slot[(size_t)t * k + j] < 0) continue;\n            int64_t e = topk_idx[(size_t)t * k + j];\n            int32_t r = (int32_t)(e / (E / R));\n            int32_t p = permuted_row(expert_offsets, expert_slot, t, j, k, e, E, R);\n            if (p >= max_rows) {\n                flags |= ORACLE_FLAG_CAPACITY;\n                continue;\n            }\n            const uint16_t* row",
+     [PERM.test_combine_permuted_term_order_is_the_topk_order]),
     ("expert drops the last weight",
      "for (int32_t j = 0; j < k; ++j) w = w + recv_topk_w[row * k + j];",
      "for (int32_t j = 0; j + 1 < k; ++j) w = w + recv_topk_w[row * k + j];",
@@ -100,7 +121,8 @@ def test_pins_catch_planted_mistake(tmp_path, monkeypatch, name, old, new, pins)
     # give the mutant the same signatures as the real library
     for sym in ("oracle_f32_to_bf16", "oracle_bf16_to_f32", "oracle_f32_to_e4m3", "oracle_e4m3_to_f32",
                 "oracle_quantize_row_e4m3", "oracle_layout", "oracle_dispatch", "oracle_restripe_prob",
-                "oracle_dispatch_nodes", "oracle_combine", "oracle_expert_scale"):
+                "oracle_dispatch_nodes", "oracle_combine", "oracle_expert_scale", "oracle_expert_layout",
+                "oracle_dispatch_permuted", "oracle_permute_received", "oracle_combine_permuted"):
         f_real, f_mut = getattr(real, sym), getattr(mutant, sym)
         f_mut.restype, f_mut.argtypes = f_real.restype, f_real.argtypes
     monkeypatch.setattr(oracle, "_lib", mutant)

@@ -8,6 +8,8 @@ combine, with R virtual EP ranks held as slabs of one GPU's HBM:
   ep_restripe_prob   prob [T][nodes][P] -> [nodes][max_tokens][P]
   ep_dispatch_nodes  node-level dense / sparse (run-length) dispatch
   ep_combine         fp32 ascending-rank gather-reduce back to token order
+  ep_get_expert_layout / ep_dispatch_permuted / ep_permute_received /
+  ep_combine_permuted  the expert-major (dispatch + permute) path, fused or split
 
 The C ABI is include/ep.h (libep_gb300.so, built in-tree by build.py); the
 functions here with the same names are its ctypes binding, and api.py
@@ -18,6 +20,8 @@ from ._lib import (  # noqa: F401
     LAYOUT_NOALLOC_SCRATCH_BYTES, EXPORTS, FLAG_BAD_EXPERT,
     FLAG_CAPACITY, FLAG_TIMEOUT, FLAG_WORKSPACE, NODES_DENSE, NODES_SPARSE, EpError, ep_combine, ep_dispatch,
     ep_dispatch_nodes, ep_get_layout, ep_get_layout_noalloc, ep_layout_workspace_size, ep_restripe_prob, lib,
+    ep_combine_permuted, ep_dispatch_permuted, ep_expert_layout_workspace_size, ep_get_expert_layout,
+    ep_permute_received,
 )
 from .api import (  # noqa: F401
     Dispatched, Layout, alloc_dispatch, alloc_layout, combine, dispatch, get_layout, read_flags,

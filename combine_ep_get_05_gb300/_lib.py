@@ -38,6 +38,8 @@ ABI_VERSION = 1
 EXPORTS = (
     "ep_abi_version", "ep_status_str", "ep_last_cuda_error", "ep_layout_workspace_size",
     "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_restripe_prob", "ep_dispatch_nodes", "ep_combine",
+    "ep_expert_layout_workspace_size", "ep_get_expert_layout", "ep_dispatch_permuted", "ep_permute_received",
+    "ep_combine_permuted",
 )
 
 
@@ -80,6 +82,12 @@ def lib():
                     "ep_restripe_prob": (i32, [P, i32, i32, i32, i32, P, P]),
                     "ep_dispatch_nodes": (i32, [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P, P]),
                     "ep_combine": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
+                    "ep_expert_layout_workspace_size": (sz, [i32, i32]),
+                    "ep_get_expert_layout": (i32, [P, i32, i32, i32, P, P, P, sz, P, P]),
+                    "ep_dispatch_permuted": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, P]),
+                    "ep_permute_received": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P,
+                                                  P, P]),
+                    "ep_combine_permuted": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]),
                 }
                 for name, (res, args) in sigs.items():
                     f = getattr(L, name)
@@ -229,3 +237,83 @@ def ep_combine(y, slot, max_tokens, out, status=None, stream=None):
     _check("status", status, torch.int32, (1,), optional=True)
     rc = lib().ep_combine(_ptr(y), _ptr(slot), T, H, R, max_tokens, _ptr(out), _ptr(status), _stream(stream))
     _done("ep_combine", rc)
+
+
+# --------------------------------------------------------------------------- expert-major path
+
+def ep_expert_layout_workspace_size(T: int, E: int) -> int:
+    return int(lib().ep_expert_layout_workspace_size(T, E))
+
+
+def ep_get_expert_layout(topk_idx, num_experts, expert_offsets, expert_slot, workspace, status=None, stream=None):
+    T, k = topk_idx.shape
+    E = num_experts
+    _check("topk_idx", topk_idx, torch.int64)
+    _check("expert_offsets", expert_offsets, torch.int32, (E + 1,))
+    _check("expert_slot", expert_slot, torch.int32, (T, k))
+    _check("workspace", workspace, torch.uint8)
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_get_expert_layout(_ptr(topk_idx), T, k, E, _ptr(expert_offsets), _ptr(expert_slot),
+                                    _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _done("ep_get_expert_layout", rc)
+
+
+def ep_dispatch_permuted(x, topk_idx, topk_w, expert_offsets, expert_slot, num_experts, num_ranks, max_rows, perm_x,
+                         perm_src=None, perm_w=None, status=None, stream=None):
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    E, R = num_experts, num_ranks
+    _check("x", x, torch.bfloat16)
+    _check("topk_idx", topk_idx, torch.int64, (T, k))
+    _check("topk_w", topk_w, torch.float32, (T, k), optional=True)
+    _check("expert_offsets", expert_offsets, torch.int32, (E + 1,))
+    _check("expert_slot", expert_slot, torch.int32, (T, k))
+    _check("perm_x", perm_x, torch.bfloat16, (R, max_rows, H))
+    _check("perm_src", perm_src, torch.int32, (R, max_rows), optional=True)
+    _check("perm_w", perm_w, torch.float32, (R, max_rows), optional=True)
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_dispatch_permuted(_ptr(x), _ptr(topk_idx), _ptr(topk_w), _ptr(expert_offsets), _ptr(expert_slot),
+                                    T, H, k, E, R, max_rows, _ptr(perm_x), _ptr(perm_src), _ptr(perm_w),
+                                    _ptr(status), _stream(stream))
+    _done("ep_dispatch_permuted", rc)
+
+
+def ep_permute_received(recv_x, recv_src_idx, recv_topk_idx, recv_topk_w, tokens_per_rank, expert_offsets,
+                        expert_slot, num_experts, max_rows, perm_x, perm_src=None, perm_w=None, status=None,
+                        stream=None):
+    R, M, H = recv_x.shape
+    k = recv_topk_idx.shape[2]
+    T = expert_slot.shape[0]
+    E = num_experts
+    _check("recv_x", recv_x, torch.bfloat16)
+    _check("recv_src_idx", recv_src_idx, torch.int32, (R, M))
+    _check("recv_topk_idx", recv_topk_idx, torch.int32, (R, M, k))
+    _check("recv_topk_w", recv_topk_w, torch.float32, (R, M, k), optional=True)
+    _check("tokens_per_rank", tokens_per_rank, torch.int32, (R,))
+    _check("expert_offsets", expert_offsets, torch.int32, (E + 1,))
+    _check("expert_slot", expert_slot, torch.int32, (T, k))
+    _check("perm_x", perm_x, torch.bfloat16, (R, max_rows, H))
+    _check("perm_src", perm_src, torch.int32, (R, max_rows), optional=True)
+    _check("perm_w", perm_w, torch.float32, (R, max_rows), optional=True)
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_permute_received(_ptr(recv_x), _ptr(recv_src_idx), _ptr(recv_topk_idx), _ptr(recv_topk_w),
+                                   _ptr(tokens_per_rank), _ptr(expert_offsets), _ptr(expert_slot), T, H, k, E, R, M,
+                                   max_rows, _ptr(perm_x), _ptr(perm_src), _ptr(perm_w), _ptr(status),
+                                   _stream(stream))
+    _done("ep_permute_received", rc)
+
+
+def ep_combine_permuted(y, topk_idx, topk_w, expert_offsets, expert_slot, num_experts, out, status=None, stream=None):
+    R, max_rows, H = y.shape
+    T, k = topk_idx.shape
+    E = num_experts
+    _check("y", y, torch.bfloat16)
+    _check("topk_idx", topk_idx, torch.int64, (T, k))
+    _check("topk_w", topk_w, torch.float32, (T, k), optional=True)
+    _check("expert_offsets", expert_offsets, torch.int32, (E + 1,))
+    _check("expert_slot", expert_slot, torch.int32, (T, k))
+    _check("out", out, torch.bfloat16, (T, H))
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_combine_permuted(_ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(expert_offsets), _ptr(expert_slot),
+                                   T, H, k, E, R, max_rows, _ptr(out), _ptr(status), _stream(stream))
+    _done("ep_combine_permuted", rc)

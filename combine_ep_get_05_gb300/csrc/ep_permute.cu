@@ -1,0 +1,642 @@
+// ep_permute.cu -- expert-major ("dispatch + permute") path: the expert layout,
+// the fused permuted dispatch, the receive-side permute of a split (hook-mode)
+// dispatch, and the combine from expert-major slabs.
+//
+// "[PR #634] Hybrid ep nixl restripe": commit "hybrid_ep: fix scan permute-fusion
+// local-experts sum array sizing" and the dispatch+permute rows of its B300
+// results -- after dispatch, each rank's tokens are permuted into local-expert
+// order using a scan over the tokens and a per-local-expert sum array.
+// "[PR #347] Feature/sm free normal kernel", 2.1 Feature: in hook mode the send
+// phase runs first and the receive phase later, as its own launch.
+//
+// Expert-major slab of rank r: rows grouped by local expert l = 0, 1, ..., E/R-1,
+// each group in token order; the row of (token t, top-k slot j) with expert e is
+//   p = expert_offsets[e] - expert_offsets[r*(E/R)] + expert_slot[t][j].
+#include <cstdio>
+
+#include "ep_common.cuh"
+
+namespace {
+
+using namespace ep;
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxExpertsPerm = 1024;  // expert layout: experts held per tile in shared memory
+constexpr int kMaxTopk = 32;
+constexpr int kUnroll = 8;
+constexpr int kBatch = 8;
+constexpr uint32_t kStateAggregate = 1u;
+constexpr uint32_t kStatePrefix = 2u;
+constexpr int kLookbackBatch = 8;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr uint32_t kWaitLimitIters = 1u << 24;
+
+__host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+inline int num_tiles_for(int T) { return T > 0 ? (T + kThreads - 1) / kThreads : 1; }
+
+__device__ __forceinline__ unsigned long long pack_word(uint32_t epoch, uint32_t state, uint32_t v) {
+    return (static_cast<unsigned long long>(epoch) << 32) | (static_cast<unsigned long long>(state) << 30) |
+           static_cast<unsigned long long>(v & 0x3fffffffu);
+}
+__device__ __forceinline__ uint32_t word_epoch(unsigned long long w) { return static_cast<uint32_t>(w >> 32); }
+__device__ __forceinline__ uint32_t word_state(unsigned long long w) { return static_cast<uint32_t>(w >> 30) & 3u; }
+__device__ __forceinline__ uint32_t word_value(unsigned long long w) { return static_cast<uint32_t>(w) & 0x3fffffffu; }
+
+// ---------------------------------------------------------------------------
+// Expert layout
+// ---------------------------------------------------------------------------
+
+struct ExpertLayoutArgs {
+    const int64_t* topk_idx;
+    int T, k, E, num_tiles;
+    int32_t* offsets;  // [E+1]
+    int32_t* eslot;    // [T][k]
+    ep_layout_ws_header_t* hdr;
+    unsigned long long* words;  // [num_tiles][E]
+    int32_t* status;
+};
+
+// expert of (t, j) if it counts (in range and the first occurrence in the row), else -1
+__device__ __forceinline__ int entry_expert(const int64_t* row, int j, int E, bool& bad) {
+    const int64_t e = row[j];
+    if (e < 0) return -1;
+    if (e >= E) {
+        bad = true;
+        return -1;
+    }
+    for (int jj = 0; jj < j; ++jj)
+        if (row[jj] == e) {
+            bad = true;
+            return -1;
+        }
+    return static_cast<int>(e);
+}
+
+// One tile of 256 tokens per CTA (thread = token). Each warp builds, per expert, the
+// 32-bit mask of its tokens that chose the expert (shared-memory atomic ORs: the result
+// does not depend on their order); a token's rank among the warp's tokens with the same
+// expert is the popcount of the mask below its lane. Per-expert tile counts are scanned
+// across tiles by a decoupled look-back over epoch-tagged words (bounded waits); the tile
+// holding the last tokens, which ends up with every expert's total, writes the offsets.
+__global__ void __launch_bounds__(kThreads, 2) expert_layout_kernel(ExpertLayoutArgs a) {
+    extern __shared__ uint32_t smem[];
+    uint32_t* s_emask = smem;                                              // [kWarps][E]
+    int32_t* s_wpref = reinterpret_cast<int32_t*>(smem + kWarps * a.E);  // [kWarps][E]
+    int32_t* s_tpref = s_wpref + kWarps * a.E;                           // [E]
+    int32_t* s_total = s_tpref + a.E;                                    // [E]
+    __shared__ uint32_t s_tile, s_epoch, s_stall, s_last;
+    __shared__ int32_t s_part[kThreads];
+
+    const int tid = static_cast<int>(threadIdx.x);
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    if (tid == 0) {
+        s_tile = atomicAdd(&a.hdr->ticket, 1u);
+        s_epoch = ld_relaxed_u32(&a.hdr->epoch) + 1u;
+        s_stall = ld_relaxed_u32(&a.hdr->stall_tile);
+    }
+    {
+        const int tg = static_cast<int>(blockIdx.x) * kThreads + tid;
+        if (tg < a.T) prefetch_l2(a.topk_idx + static_cast<size_t>(tg) * a.k);
+    }
+    for (int e = lane; e < a.E; e += 32) s_emask[warp * a.E + e] = 0u;
+    __syncthreads();
+    if (s_tile >= static_cast<uint32_t>(a.num_tiles)) {
+        if (tid == 0) raise_flag(a.status, EP_FLAG_WORKSPACE);
+        return;
+    }
+    const int tile = static_cast<int>(s_tile);
+    const uint32_t epoch = s_epoch;
+    const bool stalled = s_stall == static_cast<uint32_t>(tile) + 1u;
+    const int t = tile * kThreads + tid;
+    const int64_t* row = a.topk_idx + static_cast<size_t>(t < a.T ? t : 0) * a.k;
+
+    if (t < a.T) {
+        bool bad = false;
+        for (int j = 0; j < a.k; ++j) {
+            const int e = entry_expert(row, j, a.E, bad);
+            if (e >= 0) atomicOr(&s_emask[warp * a.E + e], 1u << lane);
+        }
+        if (bad) raise_flag(a.status, EP_FLAG_BAD_EXPERT);
+    }
+    __syncthreads();
+
+    for (int e = tid; e < a.E; e += kThreads) {
+        int run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            s_wpref[w * a.E + e] = run;
+            run += __popc(s_emask[w * a.E + e]);
+        }
+        const uint32_t agg = static_cast<uint32_t>(run);
+        unsigned long long* my_word = a.words + static_cast<size_t>(tile) * a.E + e;
+        if (!stalled) st_relaxed_u64(my_word, pack_word(epoch, tile == 0 ? kStatePrefix : kStateAggregate, agg));
+        uint32_t excl = 0;
+        bool timed_out = false;
+        int j = tile - 1;
+        while (j >= 0 && !timed_out) {
+            const int nb = j + 1 < kLookbackBatch ? j + 1 : kLookbackBatch;
+            unsigned long long wv[kLookbackBatch];
+#pragma unroll
+            for (int i = 0; i < kLookbackBatch; ++i)
+                if (i < nb) wv[i] = ld_relaxed_u64(a.words + static_cast<size_t>(j - i) * a.E + e);
+            bool found_prefix = false;
+#pragma unroll
+            for (int i = 0; i < kLookbackBatch; ++i) {
+                if (i >= nb || found_prefix || timed_out) continue;
+                const unsigned long long* p = a.words + static_cast<size_t>(j - i) * a.E + e;
+                unsigned long long w = wv[i];
+                if (word_epoch(w) != epoch || word_state(w) == 0u) {
+                    const unsigned long long start = globaltimer_ns();
+                    uint32_t polls = 0;
+                    while (word_epoch(w) != epoch || word_state(w) == 0u) {
+                        if (++polls >= kWaitLimitIters || globaltimer_ns() - start > kWaitLimitNs) {
+                            timed_out = true;
+                            break;
+                        }
+                        if (polls > 16) __nanosleep(256);
+                        w = ld_relaxed_u64(p);
+                    }
+                    if (timed_out) break;
+                }
+                excl += word_value(w);
+                if (word_state(w) == kStatePrefix) found_prefix = true;
+            }
+            if (found_prefix) break;
+            j -= nb;
+        }
+        if (timed_out) raise_flag(a.status, EP_FLAG_TIMEOUT);
+        if (tile > 0 && !stalled) st_relaxed_u64(my_word, pack_word(epoch, kStatePrefix, excl + agg));
+        s_tpref[e] = static_cast<int32_t>(excl);
+        s_total[e] = static_cast<int32_t>(excl + agg);
+    }
+    __syncthreads();
+
+    // the tile with the last tokens knows every expert's total: write the offsets
+    if (tile == a.num_tiles - 1) {
+        const int per = (a.E + kThreads - 1) / kThreads;
+        const int e0 = tid * per;
+        int sum = 0;
+        for (int i = 0; i < per; ++i)
+            if (e0 + i < a.E) sum += s_total[e0 + i];
+        // block exclusive scan of the per-thread sums (warp shuffles, then warp totals)
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(kFullMask, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) s_part[warp] = incl;
+        __syncthreads();
+        int warp_base = 0;
+        for (int w = 0; w < warp; ++w) warp_base += s_part[w];
+        int run = warp_base + incl - sum;
+        for (int i = 0; i < per; ++i) {
+            if (e0 + i < a.E) {
+                a.offsets[e0 + i] = run;
+                run += s_total[e0 + i];
+            }
+        }
+        if (tid == kThreads - 1) a.offsets[a.E] = warp_base + incl;
+    }
+
+    if (t < a.T) {
+        const uint32_t below = (1u << lane) - 1u;
+        bool bad = false;
+        for (int j = 0; j < a.k; ++j) {
+            const int e = entry_expert(row, j, a.E, bad);
+            int32_t v = -1;
+            if (e >= 0)
+                v = s_tpref[e] + s_wpref[warp * a.E + e] + __popc(s_emask[warp * a.E + e] & below);
+            a.eslot[static_cast<size_t>(t) * a.k + j] = v;
+        }
+    }
+
+    // last CTA to finish resets the ticket and advances the epoch
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&a.hdr->done, 1u) == static_cast<uint32_t>(a.num_tiles - 1);
+    __syncthreads();
+    if (s_last && tid == 0) {
+        __threadfence();
+        atomicExch(&a.hdr->ticket, 0u);
+        atomicExch(&a.hdr->done, 0u);
+        atomicExch(&a.hdr->epoch, epoch);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Row copies shared by the permuted dispatch and the receive-side permute
+// ---------------------------------------------------------------------------
+
+// copy one row of nvec 16-byte vectors to nd destination rows (row indices in s_row)
+__device__ __forceinline__ void copy_row(const uint4* src, uint4* base, const long long* s_row, int nd, int nvec) {
+    const int lane = lane_id();
+    for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
+        uint4 buf[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + u * 32 + lane;
+            if (v < nvec) buf[u] = ld_stream_v4(src + v);
+        }
+        for (int d = 0; d < nd; ++d) {
+            uint4* dst = base + static_cast<size_t>(s_row[d]) * nvec;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < nvec) st_v4(dst + v, buf[u]);
+            }
+        }
+    }
+}
+
+// Destinations of (token t): the rows of its counted top-k entries, in slot order.
+// Lane j handles slot j (k <= 32). Returns their number; s_row/s_j get row and slot.
+__device__ __forceinline__ int permuted_destinations(const int64_t* topk_idx, const int32_t* offsets,
+                                                     const int32_t* eslot, int t, int k, int E, int R,
+                                                     int max_rows, long long* s_row, int* s_j, int32_t* status) {
+    const int lane = lane_id();
+    const int epr = E / R;
+    bool ok = false, over = false;
+    long long rowi = 0;
+    if (lane < k) {
+        const int32_t sl = eslot[static_cast<size_t>(t) * k + lane];
+        const int64_t e = topk_idx[static_cast<size_t>(t) * k + lane];
+        if (sl >= 0 && e >= 0 && e < E) {
+            const int r = static_cast<int>(e) / epr;
+            const int p = offsets[e] - offsets[r * epr] + sl;
+            if (p >= 0 && p < max_rows) {
+                ok = true;
+                rowi = static_cast<long long>(r) * max_rows + p;
+            } else {
+                over = true;
+            }
+        }
+    }
+    const uint32_t m = __ballot_sync(kFullMask, ok);
+    if (ok) {
+        const int pos = __popc(m & lanemask_lt());
+        s_row[pos] = rowi;
+        s_j[pos] = lane;
+    }
+    if (__any_sync(kFullMask, over) && lane == 0) raise_flag(status, EP_FLAG_CAPACITY);
+    __syncwarp();
+    return __popc(m);
+}
+
+struct PermDispatchArgs {
+    const uint16_t* x;
+    const int64_t* topk_idx;
+    const float* topk_w;
+    const int32_t* offsets;
+    const int32_t* eslot;
+    int T, H, k, E, R, max_rows;
+    uint16_t* perm_x;
+    int32_t* perm_src;
+    float* perm_w;
+    int32_t* status;
+};
+
+// Fused dispatch + permute: warp per token, the row is read once and stored to the
+// expert-major row of each of its counted top-k entries.
+__global__ void __launch_bounds__(kThreads) dispatch_permuted_kernel(PermDispatchArgs a) {
+    __shared__ long long s_row[kWarps][kMaxTopk];
+    __shared__ int s_j[kWarps][kMaxTopk];
+    const int lane = lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int nvec = a.H / 8;
+    for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
+        const int nd = permuted_destinations(a.topk_idx, a.offsets, a.eslot, t, a.k, a.E, a.R, a.max_rows,
+                                             s_row[warp], s_j[warp], a.status);
+        if (lane < nd) {
+            const size_t row = static_cast<size_t>(s_row[warp][lane]);
+            if (a.perm_src != nullptr) a.perm_src[row] = t;
+            if (a.perm_w != nullptr) a.perm_w[row] = a.topk_w[static_cast<size_t>(t) * a.k + s_j[warp][lane]];
+        }
+        copy_row(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H),
+                 reinterpret_cast<uint4*>(a.perm_x), s_row[warp], nd, nvec);
+        __syncwarp();
+    }
+}
+
+struct PermuteRecvArgs {
+    const uint16_t* recv_x;
+    const int32_t* recv_src;
+    const int32_t* recv_tidx;
+    const float* recv_tw;
+    const int32_t* tokens_per_rank;
+    const int32_t* offsets;
+    const int32_t* eslot;
+    int T, H, k, E, R, max_tokens, max_rows;
+    uint16_t* perm_x;
+    int32_t* perm_src;
+    float* perm_w;
+    int32_t* status;
+};
+
+// Receive phase of a split dispatch: warp per received row. The CTA first turns the
+// per-rank received counts into a prefix so that warps walk only rows that exist.
+__global__ void __launch_bounds__(kThreads) permute_received_kernel(PermuteRecvArgs a) {
+    __shared__ long long s_row[kWarps][kMaxTopk];
+    __shared__ int s_j[kWarps][kMaxTopk];
+    __shared__ int s_base[257];
+    const int lane = lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int nvec = a.H / 8;
+    const int epr = a.E / a.R;
+    if (warp == 0) {  // exclusive prefix of the received counts, 32 ranks per step
+        int carry = 0;
+        for (int r0 = 0; r0 < a.R; r0 += 32) {
+            const int r = r0 + lane;
+            int c = 0;
+            if (r < a.R) {
+                c = a.tokens_per_rank[r];
+                c = c < 0 ? 0 : (c < a.max_tokens ? c : a.max_tokens);
+            }
+            int incl = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(kFullMask, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (r < a.R) s_base[r] = carry + incl - c;
+            carry += __shfl_sync(kFullMask, incl, 31);
+        }
+        if (lane == 0) s_base[a.R] = carry;
+    }
+    __syncthreads();
+    const int total = s_base[a.R];
+    for (int q = blockIdx.x * kWarps + warp; q < total; q += gridDim.x * kWarps) {
+        int lo = 0, hi = a.R;  // last r with s_base[r] <= q
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_base[mid] <= q) lo = mid;
+            else hi = mid;
+        }
+        const int r = lo;
+        const int s = q - s_base[r];
+        const size_t in_row = static_cast<size_t>(r) * a.max_tokens + s;
+        const int t = a.recv_src[in_row];
+        bool ok = false, over = false;
+        long long rowi = 0;
+        if (lane < a.k && t >= 0 && t < a.T) {
+            const int l = a.recv_tidx[in_row * a.k + lane];
+            const int32_t sl = a.eslot[static_cast<size_t>(t) * a.k + lane];
+            if (l >= 0 && l < epr && sl >= 0) {
+                const int e = r * epr + l;
+                const int p = a.offsets[e] - a.offsets[r * epr] + sl;
+                if (p >= 0 && p < a.max_rows) {
+                    ok = true;
+                    rowi = static_cast<long long>(r) * a.max_rows + p;
+                } else {
+                    over = true;
+                }
+            }
+        }
+        const uint32_t m = __ballot_sync(kFullMask, ok);
+        if (ok) {
+            const int pos = __popc(m & lanemask_lt());
+            s_row[warp][pos] = rowi;
+            s_j[warp][pos] = lane;
+        }
+        if (__any_sync(kFullMask, over) && lane == 0) raise_flag(a.status, EP_FLAG_CAPACITY);
+        __syncwarp();
+        const int nd = __popc(m);
+        if (lane < nd) {
+            const size_t row = static_cast<size_t>(s_row[warp][lane]);
+            if (a.perm_src != nullptr) a.perm_src[row] = t;
+            if (a.perm_w != nullptr) a.perm_w[row] = a.recv_tw[in_row * a.k + s_j[warp][lane]];
+        }
+        copy_row(reinterpret_cast<const uint4*>(a.recv_x + in_row * a.H), reinterpret_cast<uint4*>(a.perm_x),
+                 s_row[warp], nd, nvec);
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Combine from expert-major slabs
+// ---------------------------------------------------------------------------
+
+struct CombinePermArgs {
+    const uint16_t* y;
+    const int64_t* topk_idx;
+    const float* topk_w;  // nullable: unweighted
+    const int32_t* offsets;
+    const int32_t* eslot;
+    int T, H, k, E, R, max_rows;
+    uint16_t* out;
+    int32_t* status;
+};
+
+// Items of (token, 32 output vectors), contiguous per CTA; per item the lanes j < k
+// resolve the token's expert-major rows, then up to 8 source vectors are loaded at
+// once and accumulated strictly in slot order: acc = acc + w_j * y (one fp32 multiply
+// and one fp32 add per term, never fused), or acc = acc + y when unweighted.
+__global__ void __launch_bounds__(kThreads, 4) combine_permuted_kernel(CombinePermArgs a) {
+    __shared__ long long s_src[kWarps][kMaxTopk];
+    __shared__ float s_w[kWarps][kMaxTopk];
+    const int lane = lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int nvec = a.H / 8;
+    const int ngroups = (nvec + 31) / 32;
+    const long long items = static_cast<long long>(a.T) * ngroups;
+    const long long i0 = static_cast<long long>(blockIdx.x) * items / gridDim.x;
+    const long long i1 = static_cast<long long>(blockIdx.x + 1) * items / gridDim.x;
+    const uint4* ys = reinterpret_cast<const uint4*>(a.y);
+    uint4* os = reinterpret_cast<uint4*>(a.out);
+    const int epr = a.E / a.R;
+    for (long long it = i0 + warp; it < i1; it += kWarps) {
+        const int t = static_cast<int>(it / ngroups);
+        const int v = static_cast<int>(it - static_cast<long long>(t) * ngroups) * 32 + lane;
+        bool ok = false, over = false;
+        long long rowi = 0;
+        float wj = 1.0f;
+        if (lane < a.k) {
+            const int32_t sl = a.eslot[static_cast<size_t>(t) * a.k + lane];
+            const int64_t e = a.topk_idx[static_cast<size_t>(t) * a.k + lane];
+            if (sl >= 0 && e >= 0 && e < a.E) {
+                const int r = static_cast<int>(e) / epr;
+                const int p = a.offsets[e] - a.offsets[r * epr] + sl;
+                if (p >= 0 && p < a.max_rows) {
+                    ok = true;
+                    rowi = (static_cast<long long>(r) * a.max_rows + p) * nvec;
+                    if (a.topk_w != nullptr) wj = a.topk_w[static_cast<size_t>(t) * a.k + lane];
+                } else {
+                    over = true;
+                }
+            }
+        }
+        const uint32_t m = __ballot_sync(kFullMask, ok);
+        if (ok) {
+            const int pos = __popc(m & lanemask_lt());
+            s_src[warp][pos] = rowi;
+            s_w[warp][pos] = wj;
+        }
+        if (__any_sync(kFullMask, over) && v == lane) raise_flag(a.status, EP_FLAG_CAPACITY);
+        __syncwarp();
+        const int ns = __popc(m);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int d0 = 0; d0 < ns; d0 += kBatch) {
+            uint4 buf[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                if (d0 + i < ns && v < nvec) buf[i] = ld_stream_v4(ys + s_src[warp][d0 + i] + v);
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                if (d0 + i >= ns) continue;
+                const uint32_t wd[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+                if (a.topk_w != nullptr) {
+                    const float w = s_w[warp][d0 + i];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = __fadd_rn(acc[2 * q], __fmul_rn(bf16_lo(wd[q]), w));
+                        acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __fmul_rn(bf16_hi(wd[q]), w));
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = __fadd_rn(acc[2 * q], bf16_lo(wd[q]));
+                        acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_hi(wd[q]));
+                    }
+                }
+            }
+        }
+        if (v < nvec) {
+            uint4 o;
+            o.x = pack_bf16x2_rn(acc[0], acc[1]);
+            o.y = pack_bf16x2_rn(acc[2], acc[3]);
+            o.z = pack_bf16x2_rn(acc[4], acc[5]);
+            o.w = pack_bf16x2_rn(acc[6], acc[7]);
+            st_v4(os + static_cast<size_t>(t) * nvec + v, o);
+        }
+        __syncwarp();
+    }
+}
+
+bool g_attr_set[64] = {};
+int g_combine_per_sm[64] = {};
+
+int token_grid(long long work) {
+    const long long want = (work + kWarps - 1) / kWarps;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+}  // namespace
+
+extern "C" size_t ep_expert_layout_workspace_size(int32_t T, int32_t E) {
+    if (T < 0 || E <= 0) return 0;
+    return 256 + align256(static_cast<size_t>(num_tiles_for(T)) * E * sizeof(unsigned long long));
+}
+
+extern "C" ep_status_t ep_get_expert_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E,
+                                            int32_t* expert_offsets, int32_t* expert_slot, void* workspace,
+                                            size_t workspace_bytes, int32_t* status, void* stream) {
+    if (T < 0 || T >= (1 << 30) || k < 1 || k > kMaxTopk || E < 1 || E > kMaxExpertsPerm) return EP_ERR_INVALID;
+    if (expert_offsets == nullptr || workspace == nullptr) return EP_ERR_INVALID;
+    if (T > 0 && (topk_idx == nullptr || expert_slot == nullptr)) return EP_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EP_ERR_INVALID;
+    if (workspace_bytes < ep_expert_layout_workspace_size(T, E)) return EP_ERR_INVALID;
+    if (!aligned16_or_null(topk_idx) || !aligned16(expert_offsets) || !aligned16_or_null(expert_slot))
+        return EP_ERR_INVALID;
+    ExpertLayoutArgs a{};
+    a.topk_idx = topk_idx;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.num_tiles = num_tiles_for(T);
+    a.offsets = expert_offsets;
+    a.eslot = expert_slot;
+    a.hdr = static_cast<ep_layout_ws_header_t*>(workspace);
+    a.words = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + 256);
+    a.status = status;
+    const size_t smem = static_cast<size_t>(E) * (2 * kWarps + 2) * sizeof(int32_t);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(expert_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kMaxExpertsPerm * (2 * kWarps + 2) * static_cast<int>(sizeof(int32_t)));
+        if (err != cudaSuccess) return cuda_fail(err);
+        g_attr_set[dev] = true;
+    }
+    expert_layout_kernel<<<a.num_tiles, kThreads, smem, as_stream(stream)>>>(a);
+    return check_launch();
+}
+
+static bool perm_common_ok(int T, int H, int k, int E, int R, int max_rows) {
+    return T >= 0 && H > 0 && H % 8 == 0 && k >= 1 && k <= kMaxTopk && R >= 1 && R <= 256 && E >= R && E % R == 0 &&
+           E <= 8192 && max_rows >= 0 && static_cast<long long>(R) * max_rows <= 0x7fffffffLL;
+}
+
+extern "C" ep_status_t ep_dispatch_permuted(const void* x, const int64_t* topk_idx, const float* topk_w,
+                                            const int32_t* expert_offsets, const int32_t* expert_slot, int32_t T,
+                                            int32_t H, int32_t k, int32_t E, int32_t R, int32_t max_rows,
+                                            void* perm_x, int32_t* perm_src, float* perm_w, int32_t* status,
+                                            void* stream) {
+    if (!perm_common_ok(T, H, k, E, R, max_rows) || perm_x == nullptr) return EP_ERR_INVALID;
+    if (T == 0) return EP_OK;
+    if (x == nullptr || topk_idx == nullptr || expert_offsets == nullptr || expert_slot == nullptr ||
+        (perm_w != nullptr && topk_w == nullptr))
+        return EP_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(perm_x) || !aligned16(topk_idx) || !aligned16_or_null(topk_w) ||
+        !aligned16(expert_offsets) || !aligned16(expert_slot) || !aligned16_or_null(perm_src) ||
+        !aligned16_or_null(perm_w))
+        return EP_ERR_INVALID;
+    PermDispatchArgs a{static_cast<const uint16_t*>(x), topk_idx, topk_w, expert_offsets, expert_slot, T, H, k, E, R,
+                       max_rows, static_cast<uint16_t*>(perm_x), perm_src, perm_w, status};
+    dispatch_permuted_kernel<<<token_grid(T), kThreads, 0, as_stream(stream)>>>(a);
+    return check_launch();
+}
+
+extern "C" ep_status_t ep_permute_received(const void* recv_x, const int32_t* recv_src_idx,
+                                           const int32_t* recv_topk_idx, const float* recv_topk_w,
+                                           const int32_t* tokens_per_rank, const int32_t* expert_offsets,
+                                           const int32_t* expert_slot, int32_t T, int32_t H, int32_t k, int32_t E,
+                                           int32_t R, int32_t max_tokens, int32_t max_rows, void* perm_x,
+                                           int32_t* perm_src, float* perm_w, int32_t* status, void* stream) {
+    if (!perm_common_ok(T, H, k, E, R, max_rows) || max_tokens < 0 || perm_x == nullptr) return EP_ERR_INVALID;
+    if (T == 0 || max_tokens == 0) return EP_OK;
+    if (recv_x == nullptr || recv_src_idx == nullptr || recv_topk_idx == nullptr || tokens_per_rank == nullptr ||
+        expert_offsets == nullptr || expert_slot == nullptr || (perm_w != nullptr && recv_topk_w == nullptr))
+        return EP_ERR_INVALID;
+    if (!aligned16(recv_x) || !aligned16(perm_x) || !aligned16(recv_src_idx) || !aligned16(recv_topk_idx) ||
+        !aligned16_or_null(recv_topk_w) || !aligned16(tokens_per_rank) || !aligned16(expert_offsets) ||
+        !aligned16(expert_slot) || !aligned16_or_null(perm_src) || !aligned16_or_null(perm_w))
+        return EP_ERR_INVALID;
+    PermuteRecvArgs a{static_cast<const uint16_t*>(recv_x), recv_src_idx, recv_topk_idx, recv_topk_w, tokens_per_rank,
+                      expert_offsets, expert_slot, T, H, k, E, R, max_tokens, max_rows,
+                      static_cast<uint16_t*>(perm_x), perm_src, perm_w, status};
+    // rows received never exceed T per rank nor max_tokens
+    const long long bound = static_cast<long long>(R) * (T < max_tokens ? T : max_tokens);
+    permute_received_kernel<<<token_grid(bound), kThreads, 0, as_stream(stream)>>>(a);
+    return check_launch();
+}
+
+extern "C" ep_status_t ep_combine_permuted(const void* y, const int64_t* topk_idx, const float* topk_w,
+                                           const int32_t* expert_offsets, const int32_t* expert_slot, int32_t T,
+                                           int32_t H, int32_t k, int32_t E, int32_t R, int32_t max_rows, void* out,
+                                           int32_t* status, void* stream) {
+    if (!perm_common_ok(T, H, k, E, R, max_rows) || out == nullptr) return EP_ERR_INVALID;
+    if (T == 0) return EP_OK;
+    if (topk_idx == nullptr || expert_offsets == nullptr || expert_slot == nullptr || (max_rows > 0 && y == nullptr))
+        return EP_ERR_INVALID;
+    if (!aligned16_or_null(y) || !aligned16(out) || !aligned16(topk_idx) || !aligned16_or_null(topk_w) ||
+        !aligned16(expert_offsets) || !aligned16(expert_slot))
+        return EP_ERR_INVALID;
+    CombinePermArgs a{static_cast<const uint16_t*>(y), topk_idx, topk_w, expert_offsets, expert_slot, T, H, k, E, R,
+                      max_rows, static_cast<uint16_t*>(out), status};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int per_sm = dev >= 0 && dev < 64 ? g_combine_per_sm[dev] : 0;
+    if (per_sm == 0) {
+        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_permuted_kernel, kThreads, 0);
+        if (err != cudaSuccess) return cuda_fail(err);
+        if (per_sm < 1) per_sm = 1;
+        if (dev >= 0 && dev < 64) g_combine_per_sm[dev] = per_sm;
+    }
+    const long long items = static_cast<long long>(T) * ((H / 8 + 31) / 32);
+    const long long want = (items + kWarps - 1) / kWarps;
+    const long long cap = static_cast<long long>(sm_count()) * per_sm;
+    combine_permuted_kernel<<<static_cast<int>(want < cap ? want : cap), kThreads, 0, as_stream(stream)>>>(a);
+    return check_launch();
+}

@@ -261,6 +261,81 @@ ep_status_t ep_dispatch_nodes(const void* x, const float* prob_staging,
 ep_status_t ep_combine(const void* y, const int32_t* slot, int32_t T, int32_t H, int32_t R,
                        int32_t max_tokens, void* out, int32_t* status, void* stream);
 
+/* ------------------------------------------------------------------------- */
+/* Expert-major path: dispatch + permute (fused or split) and its combine     */
+/* ------------------------------------------------------------------------- */
+
+/* After dispatch, a rank's tokens are permuted into local-expert order for the
+ * expert GEMMs ([PR #634] commit "hybrid_ep: fix scan permute-fusion local-experts
+ * sum array sizing"; "dispatch+permute" rows of its B300 results). The expert-major
+ * slab of rank r holds its rows grouped by local expert l = 0 .. E/R-1, each group
+ * in token order; the row of (token t, top-k slot j) with expert e on rank r is
+ *   p = expert_offsets[e] - expert_offsets[r*(E/R)] + expert_slot[t][j].
+ * A token with two experts on one rank has two rows there. */
+
+/* Bytes of device workspace ep_get_expert_layout needs. */
+size_t ep_expert_layout_workspace_size(int32_t T, int32_t E);
+
+/* ep_get_expert_layout -- the per-local-expert sum array and scan:
+ *   expert_offsets[e] = number of counted (t, j) with expert e' < e   [E+1] int32
+ *   expert_slot[t][j] = number of counted (t', j') before (t, j) in token-then-slot
+ *                       order with the same expert, or -1           [T][k] int32
+ * A (t, j) counts when 0 <= topk_idx[t][j] < E and the id does not repeat an earlier
+ * slot of the same row; ids >= E and repeats get -1 and raise EP_FLAG_BAD_EXPERT.
+ *   topk_idx int64 [T][k], 1 <= k <= 32, 1 <= E <= 1024
+ *   workspace: >= ep_expert_layout_workspace_size(T, E) bytes, 256-byte aligned,
+ *     zero-filled before its first use; each completed call leaves it ready for the
+ *     next (same header and stall hook as the ep_get_layout workspace)
+ *   status: EP_FLAG_BAD_EXPERT, EP_FLAG_TIMEOUT, EP_FLAG_WORKSPACE */
+ep_status_t ep_get_expert_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E,
+                                 int32_t* expert_offsets, int32_t* expert_slot, void* workspace,
+                                 size_t workspace_bytes, int32_t* status, void* stream);
+
+/* ep_dispatch_permuted -- dispatch and permute fused (one launch): for every counted
+ * (t, j), into rank r = e / (E/R) at row p (above):
+ *   perm_x[r][p] = x[t], perm_src[r][p] = t, perm_w[r][p] = topk_w[t][j].
+ *   x bf16 [T][H] (H % 8 == 0); topk_idx int64 / topk_w fp32 [T][k];
+ *   expert_offsets / expert_slot from ep_get_expert_layout;
+ *   perm_x bf16 [R][max_rows][H]; perm_src int32 [R][max_rows] (nullable);
+ *   perm_w fp32 [R][max_rows] (nullable; needs topk_w); R * max_rows < 2^31.
+ * p >= max_rows is dropped with EP_FLAG_CAPACITY; other rows are not written. */
+ep_status_t ep_dispatch_permuted(const void* x, const int64_t* topk_idx, const float* topk_w,
+                                 const int32_t* expert_offsets, const int32_t* expert_slot,
+                                 int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
+                                 int32_t max_rows, void* perm_x, int32_t* perm_src, float* perm_w,
+                                 int32_t* status, void* stream);
+
+/* ep_permute_received -- the receive phase of a split ("hook mode", [PR #347] 2.1
+ * Feature: the send phase returns, the receive phase runs later as its own launch)
+ * dispatch: the send phase is ep_dispatch into rank slabs; this call moves each
+ * received row s < min(tokens_per_rank[r], max_tokens) of rank r, for every slot j
+ * with local id l = recv_topk_idx[r][s][j] >= 0, to the same expert-major row the
+ * fused path uses (t = recv_src_idx[r][s], e = r*(E/R) + l):
+ *   perm_x[r][p] = recv_x[r][s], perm_src[r][p] = t, perm_w[r][p] = recv_topk_w[r][s][j].
+ * The result equals ep_dispatch_permuted's. recv_* are ep_dispatch's bf16 outputs
+ * ([R][max_tokens][H], [R][max_tokens], [R][max_tokens][k] x2; recv_topk_w nullable
+ * when perm_w is NULL); tokens_per_rank from ep_get_layout. */
+ep_status_t ep_permute_received(const void* recv_x, const int32_t* recv_src_idx,
+                                const int32_t* recv_topk_idx, const float* recv_topk_w,
+                                const int32_t* tokens_per_rank, const int32_t* expert_offsets,
+                                const int32_t* expert_slot, int32_t T, int32_t H, int32_t k,
+                                int32_t E, int32_t R, int32_t max_tokens, int32_t max_rows,
+                                void* perm_x, int32_t* perm_src, float* perm_w, int32_t* status,
+                                void* stream);
+
+/* ep_combine_permuted -- combine from expert-major slabs back to token order:
+ *   out[t][h] = bf16_rn(acc), acc = 0; for j = 0 .. k-1 with a counted (t, j):
+ *       acc = acc + topk_w[t][j] * float(y[r][p][h])   (topk_w given: one fp32
+ *                                                        multiply, one fp32 add)
+ *       acc = acc + float(y[r][p][h])                  (topk_w NULL)
+ * in exactly that order, so the result is deterministic. Rows p >= max_rows were
+ * never written: skipped with EP_FLAG_CAPACITY. A token with no counted entry gets +0.
+ *   y bf16 [R][max_rows][H]; out bf16 [T][H]. */
+ep_status_t ep_combine_permuted(const void* y, const int64_t* topk_idx, const float* topk_w,
+                                const int32_t* expert_offsets, const int32_t* expert_slot,
+                                int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
+                                int32_t max_rows, void* out, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,159 @@
+"""GPU parity of the expert-major path against the oracle, bit for bit: the expert
+layout, the fused dispatch + permute, the receive-side permute of a split dispatch
+(whose result must equal the fused one), and the combine from expert-major slabs,
+weighted and unweighted. Output buffers sit between guard regions."""
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_get_05_gb300 as ep
+import oracle
+import workloads
+from gpu_helpers import SENT_BF16, SENT_F32, SENT_I32, check_guards, dev_bf16, gpu_layout, guarded, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ep.build_library()
+    ep.lib()
+
+
+def gpu_expert_layout(topk, E, ws=None):
+    T, k = topk.shape
+    off = torch.full((E + 1,), -9, dtype=torch.int32, device="cuda")
+    slot = torch.full((T, k), -9, dtype=torch.int32, device="cuda")
+    if ws is None:
+        ws = torch.zeros(max(256, ep.ep_expert_layout_workspace_size(T, E)), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_get_expert_layout(topk, E, off, slot, ws, status)
+    return off, slot, ws, status
+
+
+def check_expert_layout(w, topk_np=None):
+    topk_np = w.topk_idx if topk_np is None else topk_np
+    EL = oracle.expert_layout(topk_np, w.E)
+    off, slot, ws, status = gpu_expert_layout(torch.from_numpy(topk_np).cuda(), w.E)
+    assert np.array_equal(host_bits(off), EL["expert_offsets"])
+    assert np.array_equal(host_bits(slot), EL["expert_slot"])
+    assert int(status.item()) == EL["flags"]
+    return EL, off, slot
+
+
+def run_permuted(w, max_rows=None, weighted=True):
+    E, R, T, H, k = w.E, w.R, w.T, w.H, w.k
+    EL, off, slot = check_expert_layout(w)
+    rows = oracle.rows_per_rank(EL["expert_offsets"], E, R)
+    M = max_rows if max_rows is not None else max(1, int(rows.max()))
+    x = dev_bf16(w.x)
+    topk = torch.from_numpy(w.topk_idx).cuda()
+    tw = torch.from_numpy(w.topk_w).cuda()
+
+    # fused dispatch + permute
+    px, bpx = guarded((R, M, H), torch.bfloat16, SENT_BF16)
+    ps, bps = guarded((R, M), torch.int32, SENT_I32)
+    pw, bpw = guarded((R, M), torch.float32, SENT_F32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_dispatch_permuted(x, topk, tw, off, slot, E, R, M, px, ps, pw, st)
+    ref = oracle.dispatch_permuted(w.x, w.topk_idx, w.topk_w, EL, E, R, M, fill_x=SENT_BF16, fill_idx=SENT_I32,
+                                   fill_w=SENT_F32)
+    assert int(st.item()) == ref["flags"]
+    assert np.array_equal(host_bits(px), ref["perm_x"])
+    assert np.array_equal(host_bits(ps), ref["perm_src"])
+    assert np.array_equal(host_bits(pw).view(np.uint32), ref["perm_w"].view(np.uint32))
+    for b, v, f in ((bpx, px, SENT_BF16), (bps, ps, SENT_I32), (bpw, pw, SENT_F32)):
+        check_guards(b, v.numel(), f)
+
+    # split: rank-level dispatch (send), then the receive-side permute
+    L = oracle.layout(w.topk_idx, E, R, w.ranks_per_node)
+    Mr = max(1, int(L["tokens_per_rank"].max()))
+    topk_d, lay = gpu_layout(w)
+    d = ep.alloc_dispatch(R, Mr, H, k)
+    ep.dispatch(x, topk_d, tw, lay, Mr, out=d)
+    sx, bsx = guarded((R, M, H), torch.bfloat16, SENT_BF16)
+    ss, bss = guarded((R, M), torch.int32, SENT_I32)
+    sw, bsw = guarded((R, M), torch.float32, SENT_F32)
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_permute_received(d.recv_x, d.recv_src_idx, d.recv_topk_idx, d.recv_topk_w, lay.tokens_per_rank, off, slot,
+                           E, M, sx, ss, sw, st2)
+    assert int(st2.item()) == ref["flags"]
+    assert np.array_equal(host_bits(sx), ref["perm_x"])
+    assert np.array_equal(host_bits(ss), ref["perm_src"])
+    assert np.array_equal(host_bits(sw).view(np.uint32), ref["perm_w"].view(np.uint32))
+    for b, v, f in ((bsx, sx, SENT_BF16), (bss, ss, SENT_I32), (bsw, sw, SENT_F32)):
+        check_guards(b, v.numel(), f)
+
+    # combine from the slabs: random expert outputs (seeded), weighted and plain
+    y_np = workloads.random_bf16_rows(17, (R, M, H))
+    y = dev_bf16(y_np)
+    for wts in (((tw, w.topk_w),) if weighted else ()) + ((None, None),):
+        out, bout = guarded((T, H), torch.bfloat16, SENT_BF16)
+        st3 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ep.ep_combine_permuted(y, topk, wts[0], off, slot, E, out, st3)
+        exp, flags = oracle.combine_permuted(y_np, w.topk_idx, wts[1], EL, E, R)
+        assert int(st3.item()) == flags
+        assert np.array_equal(host_bits(out), exp)
+        check_guards(bout, out.numel(), SENT_BF16)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", {}),
+    ("tiny", {"T": 1}),
+    ("dsv3", {"T": 1000, "H": 1024}),
+    ("dsv3", {"T": 777, "H": 7168}),
+    ("skewed", {"T": 3000, "H": 256}),
+    ("restripe", {"T": 600, "H": 128}),
+])
+def test_permuted_path_matches_oracle(name, over):
+    run_permuted(workloads.make(name, **over))
+
+
+def test_permuted_path_full_size_dsv3():
+    run_permuted(workloads.make("dsv3"))
+
+
+def test_permuted_capacity_overflow():
+    w = workloads.make("skewed", T=2000, H=64)
+    EL = oracle.expert_layout(w.topk_idx, w.E)
+    rows = oracle.rows_per_rank(EL["expert_offsets"], w.E, w.R)
+    run_permuted(w, max_rows=int(rows.max()) // 2)
+
+
+def test_expert_layout_edge_cases():
+    rng = np.random.Generator(np.random.PCG64(31))
+    # repeats, out-of-range ids and empty slots are dropped and flagged
+    w = workloads.make("tiny", T=700, H=8)
+    t = w.topk_idx.copy()
+    t[3, 1] = t[3, 0]
+    t[10, 2] = w.E + 5
+    t[20, :] = -1
+    check_expert_layout(w, t)
+    # the largest expert count, k = 32, several tiles with a ragged tail
+    topk = workloads.routing_uniform(rng, 1537, 1024, 32)
+    w2 = workloads.make("tiny", T=1537, H=8, E=1024, k=32, R=4)
+    check_expert_layout(w2, topk)
+    # empty batch
+    off, slot, ws, status = gpu_expert_layout(torch.zeros((0, 4), dtype=torch.int64, device="cuda"), 16)
+    assert np.all(host_bits(off) == 0) and int(status.item()) == 0
+
+
+def test_expert_layout_workspace_reuse_and_bounded_wait():
+    w = workloads.make("dsv3", T=256 * 5, H=8)
+    topk = torch.from_numpy(w.topk_idx).cuda()
+    EL = oracle.expert_layout(w.topk_idx, w.E)
+    off, slot, ws, status = gpu_expert_layout(topk, w.E)
+    ws[12:16].copy_(torch.tensor([3, 0, 0, 0], dtype=torch.uint8))  # tile 2 never publishes
+    status.zero_()
+    ep.ep_get_expert_layout(topk, w.E, off, slot, ws, status)
+    assert int(status.item()) & ep.FLAG_TIMEOUT
+    ws[12:16].zero_()
+    for T in (1280, 300, 1):  # the same workspace keeps working, whatever T
+        status.zero_()
+        ep.ep_get_expert_layout(topk[:T], w.E, off, slot[:T], ws, status)
+        ELT = oracle.expert_layout(w.topk_idx[:T], w.E)
+        assert np.array_equal(host_bits(off), ELT["expert_offsets"])
+        assert np.array_equal(host_bits(slot[:T]), ELT["expert_slot"])
+        assert int(status.item()) == 0

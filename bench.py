@@ -504,6 +504,42 @@ def extra_stages(ep, dev, args, flush, peak):
         res[name] = gbs(T * 2 * H + dests * (2 * H + 2 * P * 4) + (T * Nn if mode == ep.NODES_SPARSE else 0), ms)
     del rx, rp, staging, prob, x, lay
 
+    # expert-major path on the dsv3 shape: expert layout, fused dispatch + permute, the split
+    # path's receive phase, and the weighted combine from the expert-major slabs
+    w = workloads.make("dsv3")
+    T, H, k, E, R = w.T, w.H, w.k, w.E, w.R
+    x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(w.topk_idx).to(dev)
+    tw = torch.from_numpy(w.topk_w).to(dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    eslot = torch.empty((T, k), dtype=torch.int32, device=dev)
+    ews = torch.zeros(ep.ep_expert_layout_workspace_size(T, E), dtype=torch.uint8, device=dev)
+    ep.ep_get_expert_layout(topk, E, off, eslot, ews)
+    offs = off.cpu().numpy()
+    epr = E // R
+    Mp = int(max(offs[(r + 1) * epr] - offs[r * epr] for r in range(R)))
+    entries = int(offs[E])
+    px = torch.empty((R, Mp, H), dtype=torch.bfloat16, device=dev)
+    ps = torch.empty((R, Mp), dtype=torch.int32, device=dev)
+    pw = torch.empty((R, Mp), dtype=torch.float32, device=dev)
+    lay = ep.get_layout(topk, E, R, w.ranks_per_node)
+    pairs = int(lay.tokens_per_rank.sum().item())
+    d = ep.alloc_dispatch(R, w.max_tokens, H, k, device=dev)
+    ep.dispatch(x, topk, tw, lay, w.max_tokens, out=d)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ms = time_events(lambda: ep.ep_get_expert_layout(topk, E, off, eslot, ews), n, flush, stream)
+    res["expert_layout"] = gbs(T * k * 12 + 4 * (E + 1), ms)
+    ms = time_events(lambda: ep.ep_dispatch_permuted(x, topk, tw, off, eslot, E, R, Mp, px, ps, pw), n, flush, stream)
+    res["dispatch_permuted"] = gbs(T * 2 * H + T * k * 16 + entries * (2 * H + 8), ms)
+    ms = time_events(lambda: ep.ep_permute_received(d.recv_x, d.recv_src_idx, d.recv_topk_idx, d.recv_topk_w,
+                                                    lay.tokens_per_rank, off, eslot, E, Mp, px, ps, pw),
+                     n, flush, stream)
+    res["permute_received"] = gbs(pairs * (2 * H + 4 + 8 * k) + T * k * 4 + entries * (2 * H + 8), ms)
+    ms = time_events(lambda: ep.ep_combine_permuted(px, topk, tw, off, eslot, E, out), n, flush, stream)
+    res["combine_permuted_weighted"] = gbs(entries * 2 * H + T * k * 16 + T * 2 * H, ms)
+    res["permuted_entries"] = entries
+    del px, ps, pw, d, x, lay, out
+
     # skewed routing dispatch + combine (T=16384, H=4096, R=64, max_tokens = hottest rank)
     w = workloads.make("skewed")
     x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)

@@ -135,6 +135,24 @@ __global__ void __launch_bounds__(kThreads, 2) dispatch_bf16_kernel(DispatchArgs
     }
 }
 
+// x / scale, correctly rounded to fp32, as far as its E4M3 rounding can tell. The
+// E4M3 code of a quotient only changes where the quotient crosses a midpoint
+// between two E4M3 values. y = x * RN(1/scale) is within 3 ulp of RN(x / scale)
+// (three roundings -- of 1/scale, of the product, of the exact quotient -- each at
+// most half an ulp of relative error, and an ulp is at least 2^-24 of the value),
+// so whenever y is
+// more than 8 ulp away from every midpoint the two quotients round to the same
+// code and y is used. For a normal E4M3 binade the midpoints are the fp32 values
+// whose 20 mantissa bits below the 3 E4M3 mantissa bits read 0x80000; below 2^-6
+// (the E4M3 subnormals) and near a midpoint the exact division decides.
+__device__ __forceinline__ float quotient(float x, float scale, float rcp) {
+    const float y = __fmul_rn(x, rcp);
+    const uint32_t b = __float_as_uint(y) & 0x7fffffffu;
+    const uint32_t low = b & 0xfffffu;
+    const bool near_midpoint = low - 0x7fff8u < 16u;
+    return (b < 0x3c800000u || near_midpoint) ? __fdiv_rn(x, scale) : y;
+}
+
 // One 128-element block is held by 8 lanes, 16 bf16 (two 16-byte vectors) per
 // lane. Returns the lane's 16 E4M3 codes as one 16-byte vector (element i in
 // byte i) and the block's scale (the same in all 8 lanes).
@@ -160,6 +178,11 @@ __device__ __forceinline__ void quantize16(const uint4& a, const uint4& b, uint4
         for (int i = 0; i < 8; ++i)
             c[i] = ((__float_as_uint(f[2 * i]) >> 31) ? 0x80u : 0u) |
                    ((__float_as_uint(f[2 * i + 1]) >> 31) ? 0x8000u : 0u);
+    } else if (scale >= 1.17549435e-38f) {  // 1/scale is finite: quotient by multiplication
+        const float rcp = __frcp_rn(scale);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            c[i] = ep::pack_e4m3x2_rn_sat(quotient(f[2 * i], scale, rcp), quotient(f[2 * i + 1], scale, rcp));
     } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -175,7 +198,7 @@ __device__ __forceinline__ void quantize16(const uint4& a, const uint4& b, uint4
 // elements 16*(l % 8) .. +15 of block l / 8, so every code store is one 16-byte
 // vector per lane (512 bytes per warp instruction) and the 4 scales of an
 // iteration leave in one 16-byte store when they are 16-byte aligned.
-__global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a) {
+__global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a, int interleave) {
     __shared__ int s_rank[kWarps][kMaxDest];
     __shared__ long long s_row[kWarps][kMaxDest];
     const int lane = ep::lane_id();
@@ -186,7 +209,10 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a) 
     const bool vec_scales = (nblk & 3) == 0;
     uint8_t* recv = static_cast<uint8_t*>(a.recv_x);
 
-    for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
+    // one wave: token c + G*w goes to warp w of CTA c, so every SM gets the same number of
+    // tokens; several waves: consecutive tokens per CTA and the hardware balances CTAs
+    for (int t = interleave ? static_cast<int>(blockIdx.x + gridDim.x * warp) : static_cast<int>(blockIdx.x) * kWarps + warp;
+         t < a.T; t += gridDim.x * kWarps) {
         const int nd = gather_destinations(a, t, s_rank[warp], s_row[warp]);
         write_metadata(a, t, nd, s_rank[warp], s_row[warp]);
         const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H);
@@ -236,6 +262,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a) 
     }
 }
 
+int g_fp8_per_sm[64] = {};
+
 int grid_for(int T, int blocks_per_sm) {
     const int want = (T + kWarps - 1) / kWarps;
     const int cap = ep::sm_count() * blocks_per_sm;
@@ -283,10 +311,22 @@ extern "C" ep_status_t ep_dispatch(const void* x, ep_dtype_t out_dtype, const in
     a.recv_topk_idx = recv_topk_idx;
     a.recv_topk_w = recv_topk_w;
     a.status = status;
-    const int grid = grid_for(T, 8);
-    if (fp8)
-        dispatch_fp8_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(a);
-    else
-        dispatch_bf16_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(a);
+    if (fp8) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int per_sm = dev >= 0 && dev < 64 ? g_fp8_per_sm[dev] : 0;
+        if (per_sm == 0) {
+            cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fp8_kernel, kThreads, 0);
+            if (err != cudaSuccess) return cuda_fail(err);
+            if (per_sm < 1) per_sm = 1;
+            if (dev >= 0 && dev < 64) g_fp8_per_sm[dev] = per_sm;
+        }
+        const long long resident = static_cast<long long>(sm_count()) * per_sm;
+        const bool one_wave = static_cast<long long>(T) <= resident * kWarps;
+        const int grid = one_wave ? static_cast<int>(resident) : grid_for(T, 8);
+        dispatch_fp8_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(a, one_wave ? 1 : 0);
+    } else {
+        dispatch_bf16_kernel<<<grid_for(T, 8), kThreads, 0, as_stream(stream)>>>(a);
+    }
     return check_launch();
 }

@@ -83,9 +83,10 @@ def load_peaks():
 
 
 def source_digest(name):
-    path = os.path.join(ROOT, "combine_ep_get_05_gb300", "csrc", name)
+    """Hash of a kernel's translation unit and every shared internal header."""
+    csrc = os.path.join(ROOT, "combine_ep_get_05_gb300", "csrc")
     h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "combine_ep_get_05_gb300", "csrc", "ep_common.cuh")):
+    for p in [os.path.join(csrc, name)] + sorted(os.path.join(csrc, f) for f in os.listdir(csrc) if f.endswith(".cuh")):
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -357,7 +358,7 @@ def run_ours(args, world, rank):
     peak, peak_kind = load_peaks()
     mean = {s: statistics.mean(v) for s, v in stage_ms.items()}
     dom = max(("dispatch", "combine"), key=lambda s: mean[s])
-    dom_kernel = {"dispatch": "dispatch_bf16_kernel", "combine": "combine_kernel"}[dom]
+    dom_kernel = {"dispatch": "scatter_rows_tma_kernel<DispatchScatter>", "combine": "combine_kernel"}[dom]
     dom_src = {"dispatch": "ep_dispatch.cu", "combine": "ep_combine.cu"}[dom]
     achieved = b[dom] / (mean[dom] * 1e-3) / 1e9
     traffic, traffic_note = committed_traffic(dom_kernel, dom_src)

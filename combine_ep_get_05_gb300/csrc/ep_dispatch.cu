@@ -4,8 +4,8 @@
 // FP8 and BF16 dispatch of 3.2.1), with the optional per-token 1x128 E4M3
 // quantisation fused into the copy.
 //
-// bf16 rows move with bulk asynchronous copies (dispatch_bf16_tma_kernel, below); the
-// register kernel described next serves rows too large for three shared-memory buffers
+// bf16 rows move with bulk asynchronous copies (the shared scatter of ep_scatter.cuh); the
+// register kernel described next serves rows too large for its shared-memory buffers
 // and, with the quantisation added, the FP8 path.
 //
 // Register design: a persistent grid of warps, one token per warp at a time. The warp
@@ -18,6 +18,7 @@
 // destination. Nothing here is a contraction, so no tensor cores: the kernel
 // is bound by HBM bandwidth (read T rows, write one row per (token, rank)).
 #include "ep_common.cuh"
+#include "ep_scatter.cuh"
 
 namespace {
 
@@ -157,78 +158,23 @@ __device__ __forceinline__ float quotient(float x, float scale, float rcp) {
     return (b < 0x3c800000u || near_midpoint) ? __fdiv_rn(x, scale) : y;
 }
 
-// bf16 dispatch with bulk asynchronous copies (TMA): one warp per CTA and three row
-// buffers in shared memory. Lane 0 streams the CTA's tokens (t = blockIdx.x, +gridDim.x,
-// ...) into the buffers with bulk global->shared copies that complete on an mbarrier,
-// two rows ahead of use, and sends each row to every destination slab with one bulk
-// shared->global copy per destination; a buffer is refilled only once the bulk stores
-// that read it have finished reading. The other lanes gather destinations and write the
-// metadata meanwhile. No row data passes through registers, so the LSU queue that limits
-// the register kernel stays free; the grid oversubscribes the SMs about 8 times so the
-// hardware block scheduler balances tokens with different numbers of destinations. Every
-// barrier wait is bounded: on timeout the kernel drains its own outstanding loads,
-// raises EP_FLAG_TIMEOUT and stops.
-constexpr int kTmaStages = 3;
-constexpr int kTmaOversubscribe = 8;
-constexpr size_t kTmaMaxSmem = 200 * 1024;
-
-__global__ void __launch_bounds__(32) dispatch_bf16_tma_kernel(DispatchArgs a) {
-    extern __shared__ __align__(128) unsigned char s_rows[];
-    __shared__ __align__(8) uint64_t s_bar[kTmaStages];
-    __shared__ int s_rank[kMaxDest];
-    __shared__ long long s_row[kMaxDest];
-    const int lane = ep::lane_id();
-    const uint32_t rowb = static_cast<uint32_t>(a.H) * 2u;
-    const int n_my = static_cast<int>(blockIdx.x) < a.T ? (a.T - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
-    char* recv = static_cast<char*>(a.recv_x);
-    auto token = [&](int j) { return static_cast<int>(blockIdx.x) + j * static_cast<int>(gridDim.x); };
-    int issued = 0;  // loads issued by lane 0 (tokens 0 .. issued-1 of this CTA)
-    if (lane == 0) {
-        for (int st = 0; st < kTmaStages; ++st) ep::mbar_init(&s_bar[st], 1);
-        ep::mbar_init_fence();
-        for (; issued < kTmaStages - 1 && issued < n_my; ++issued) {
-            ep::mbar_arrive_expect_tx(&s_bar[issued], rowb);
-            ep::bulk_load(s_rows + static_cast<size_t>(issued) * rowb, a.x + static_cast<size_t>(token(issued)) * a.H,
-                          rowb, &s_bar[issued]);
-        }
+// bf16 dispatch through the shared bulk-copy scatter (ep_scatter.cuh): source row t is
+// x[t], its destinations are the compacted slot row, the side work is the metadata.
+struct DispatchScatter {
+    DispatchArgs a;
+    char* dst;
+    uint32_t row_bytes;
+    int32_t* status;
+    __device__ int items() const { return a.T; }
+    __device__ const void* source(int t) const { return a.x + static_cast<size_t>(t) * a.H; }
+    __device__ int destinations(int t, long long* rows, int* aux) const {
+        return gather_destinations(a, t, aux, rows);
     }
-    __syncwarp();
-    int j = 0;
-    bool ok = true;
-    for (; j < n_my && ok; ++j) {
-        const int t = token(j);
-        const int st = j % kTmaStages;
-        const int nd = gather_destinations(a, t, s_rank, s_row);
-        write_metadata(a, t, nd, s_rank, s_row);
-        if (lane == 0) {
-            if (issued < n_my && issued == j + kTmaStages - 1) {
-                ep::bulk_wait_read_all();  // the buffer of token j-1 is free once its stores have read it
-                const int sn = issued % kTmaStages;
-                ep::mbar_arrive_expect_tx(&s_bar[sn], rowb);
-                ep::bulk_load(s_rows + static_cast<size_t>(sn) * rowb, a.x + static_cast<size_t>(token(issued)) * a.H,
-                              rowb, &s_bar[sn]);
-                ++issued;
-            }
-            ok = ep::mbar_wait_bounded(&s_bar[st], static_cast<uint32_t>((j / kTmaStages) & 1));
-            if (ok) {
-                const unsigned char* buf = s_rows + static_cast<size_t>(st) * rowb;
-                for (int d = 0; d < nd; ++d) ep::bulk_store(recv + static_cast<size_t>(s_row[d]) * rowb, buf, rowb);
-                ep::bulk_commit();
-            }
-        }
-        ok = __shfl_sync(ep::kFullMask, ok, 0);
-        __syncwarp();
+    __device__ void side_work(int t, int nd, const long long* rows, const int* aux) const {
+        write_metadata(a, t, nd, aux, rows);
     }
-    if (lane == 0) {
-        ep::bulk_wait_all();
-        if (!ok) {
-            // token j-1 timed out: wait (bounded) for every load still in flight before leaving
-            for (int i = j - 1; i < issued; ++i)
-                (void)ep::mbar_wait_bounded(&s_bar[i % kTmaStages], static_cast<uint32_t>((i / kTmaStages) & 1));
-            ep::raise_flag(a.status, EP_FLAG_TIMEOUT);
-        }
-    }
-}
+    __device__ void prologue() const {}
+};
 
 // One 128-element block is held by 8 lanes, 16 bf16 (two 16-byte vectors) per
 // lane. Returns the lane's 16 E4M3 codes as one 16-byte vector (element i in
@@ -340,7 +286,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a, 
 }
 
 int g_fp8_per_sm[64] = {};
-bool g_tma_attr_set[64] = {};
 
 int grid_for(int T, int blocks_per_sm) {
     const int want = (T + kWarps - 1) / kWarps;
@@ -403,23 +348,10 @@ extern "C" ep_status_t ep_dispatch(const void* x, ep_dtype_t out_dtype, const in
         const bool one_wave = static_cast<long long>(T) <= resident * kWarps;
         const int grid = one_wave ? static_cast<int>(resident) : grid_for(T, 8);
         dispatch_fp8_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(a, one_wave ? 1 : 0);
-    } else if (static_cast<size_t>(kTmaStages) * H * 2 <= kTmaMaxSmem) {
-        const size_t smem = static_cast<size_t>(kTmaStages) * H * 2;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !g_tma_attr_set[dev]) {
-            cudaError_t err = cudaFuncSetAttribute(dispatch_bf16_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(kTmaMaxSmem));
-            if (err != cudaSuccess) return cuda_fail(err);
-            g_tma_attr_set[dev] = true;
-        }
-        int per_sm = 0;
-        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_bf16_tma_kernel, 32, smem);
-        if (err != cudaSuccess) return cuda_fail(err);
-        const long long cap = static_cast<long long>(sm_count()) * (per_sm > 0 ? per_sm : 1) * kTmaOversubscribe;
-        const int grid = static_cast<int>(T < cap ? T : cap);
-        dispatch_bf16_tma_kernel<<<grid, 32, smem, as_stream(stream)>>>(a);
     } else {
+        const DispatchScatter sp{a, static_cast<char*>(recv_x), static_cast<uint32_t>(H) * 2u, status};
+        const ep_status_t st = launch_scatter_rows(sp, T, as_stream(stream));
+        if (st != EP_ERR_INVALID) return st;  // rows too large for the shared-memory buffers: registers
         dispatch_bf16_kernel<<<grid_for(T, 8), kThreads, 0, as_stream(stream)>>>(a);
     }
     return check_launch();

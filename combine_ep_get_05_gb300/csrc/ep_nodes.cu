@@ -14,6 +14,7 @@
 // with ballots over 32 tokens at a time (a run starts where a bit is set and
 // the bit before it, carried across groups, is clear).
 #include "ep_common.cuh"
+#include "ep_scatter.cuh"
 
 namespace {
 
@@ -108,6 +109,77 @@ __global__ void __launch_bounds__(kThreads) node_dispatch_kernel(NodeArgs a) {
     }
 }
 
+// Run count of (node n, chunk c) for q = n * nchunks + c, one warp: ballots over 32
+// tokens at a time; a run starts where a bit is set and the bit before it (carried
+// across groups) is clear.
+__device__ __forceinline__ void count_runs(const NodeArgs& a, int q) {
+    const int lane = ep::lane_id();
+    const int n = q / a.nchunks;
+    const int c = q - n * a.nchunks;
+    const int t0 = c * a.chunk;
+    const int t1 = t0 + a.chunk < a.T ? t0 + a.chunk : a.T;
+    int runs = 0;
+    if (a.dense) {
+        runs = t1 > t0 ? 1 : 0;
+    } else {
+        uint32_t carry = 0;
+        for (int g = t0; g < t1; g += 32) {
+            const int t = g + lane;
+            const bool in = t < t1 && a.in_node[static_cast<size_t>(t) * a.N + n] != 0;
+            const uint32_t m = __ballot_sync(ep::kFullMask, in);
+            runs += __popc(m & ~((m << 1) | carry));
+            carry = m >> 31;
+        }
+    }
+    if (lane == 0) a.num_runs[q] = runs;
+}
+
+// Node dispatch through the shared bulk-copy scatter (ep_scatter.cuh): token t goes to
+// row t of every destination node; the side work copies the token's staged prob slice
+// to each destination, and the prologue counts the runs.
+struct NodeScatter {
+    NodeArgs a;
+    char* dst;
+    uint32_t row_bytes;
+    int32_t* status;
+    __device__ int items() const { return a.T; }
+    __device__ const void* source(int t) const { return a.x + static_cast<size_t>(t) * a.H; }
+    __device__ int destinations(int t, long long* rows, int* aux) const {
+        const int lane = ep::lane_id();
+        int nd = 0;
+        for (int n0 = 0; n0 < a.N; n0 += 32) {
+            const int n = n0 + lane;
+            const bool go = n < a.N && (a.dense || a.in_node[static_cast<size_t>(t) * a.N + n] != 0);
+            const uint32_t m = __ballot_sync(ep::kFullMask, go);
+            if (go) {
+                const int pos = nd + __popc(m & ep::lanemask_lt());
+                rows[pos] = static_cast<long long>(n) * a.max_tokens + t;
+                aux[pos] = n;
+            }
+            nd += __popc(m);
+        }
+        __syncwarp();
+        return nd;
+    }
+    __device__ void side_work(int t, int nd, const long long* rows, const int* aux) const {
+        if (a.recv_prob == nullptr) return;
+        const int lane = ep::lane_id();
+        const int pvec = a.P / 4;
+        for (int d = 0; d < nd; ++d) {
+            const size_t row = static_cast<size_t>(rows[d]);
+            const uint4* ps = reinterpret_cast<const uint4*>(a.staging + row * a.P);
+            uint4* pd = reinterpret_cast<uint4*>(a.recv_prob + row * a.P);
+            for (int v = lane; v < pvec; v += 32) ep::st_v4(pd + v, ep::ld_stream_v4(ps + v));
+        }
+        (void)t;
+        (void)aux;
+    }
+    __device__ void prologue() const {
+        if (a.num_runs == nullptr) return;
+        for (int q = static_cast<int>(blockIdx.x); q < a.N * a.nchunks; q += static_cast<int>(gridDim.x)) count_runs(a, q);
+    }
+};
+
 }  // namespace
 
 extern "C" ep_status_t ep_dispatch_nodes(const void* x, const float* prob_staging, const uint8_t* is_token_in_node,
@@ -143,6 +215,9 @@ extern "C" ep_status_t ep_dispatch_nodes(const void* x, const float* prob_stagin
     a.recv_x = static_cast<uint16_t*>(recv_x_node);
     a.recv_prob = with_prob ? recv_prob_node : nullptr;
     a.num_runs = num_runs;
+    const NodeScatter sp{a, static_cast<char*>(recv_x_node), static_cast<uint32_t>(H) * 2u, nullptr};
+    const ep_status_t st = launch_scatter_rows(sp, T, as_stream(stream));
+    if (st != EP_ERR_INVALID) return st;  // rows too large for the shared-memory buffers: registers
     const long long work = static_cast<long long>(T) > static_cast<long long>(num_nodes) * a.nchunks
                                ? T
                                : static_cast<long long>(num_nodes) * a.nchunks;

@@ -15,6 +15,7 @@
 #include <cstdio>
 
 #include "ep_common.cuh"
+#include "ep_scatter.cuh"
 
 namespace {
 
@@ -319,6 +320,29 @@ __global__ void __launch_bounds__(kThreads) dispatch_permuted_kernel(PermDispatc
     }
 }
 
+// the fused dispatch + permute through the shared bulk-copy scatter (ep_scatter.cuh)
+struct PermScatter {
+    PermDispatchArgs a;
+    char* dst;
+    uint32_t row_bytes;
+    int32_t* status;
+    __device__ int items() const { return a.T; }
+    __device__ const void* source(int t) const { return a.x + static_cast<size_t>(t) * a.H; }
+    __device__ int destinations(int t, long long* rows, int* aux) const {
+        return permuted_destinations(a.topk_idx, a.offsets, a.eslot, t, a.k, a.E, a.R, a.max_rows, rows, aux,
+                                     a.status);
+    }
+    __device__ void side_work(int t, int nd, const long long* rows, const int* aux) const {
+        const int lane = lane_id();
+        if (lane < nd) {
+            const size_t row = static_cast<size_t>(rows[lane]);
+            if (a.perm_src != nullptr) a.perm_src[row] = t;
+            if (a.perm_w != nullptr) a.perm_w[row] = a.topk_w[static_cast<size_t>(t) * a.k + aux[lane]];
+        }
+    }
+    __device__ void prologue() const {}
+};
+
 struct PermuteRecvArgs {
     const uint16_t* recv_x;
     const int32_t* recv_src;
@@ -584,6 +608,9 @@ extern "C" ep_status_t ep_dispatch_permuted(const void* x, const int64_t* topk_i
         return EP_ERR_INVALID;
     PermDispatchArgs a{static_cast<const uint16_t*>(x), topk_idx, topk_w, expert_offsets, expert_slot, T, H, k, E, R,
                        max_rows, static_cast<uint16_t*>(perm_x), perm_src, perm_w, status};
+    const PermScatter sp{a, static_cast<char*>(perm_x), static_cast<uint32_t>(H) * 2u, status};
+    const ep_status_t st = launch_scatter_rows(sp, T, as_stream(stream));
+    if (st != EP_ERR_INVALID) return st;  // rows too large for the shared-memory buffers: registers
     dispatch_permuted_kernel<<<token_grid(T), kThreads, 0, as_stream(stream)>>>(a);
     return check_launch();
 }

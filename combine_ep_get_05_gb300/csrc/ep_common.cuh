@@ -76,6 +76,13 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
     return v;
 }
 
+// Returns the old value; release covers the writes that a preceding __syncthreads
+// ordered before it, acquire makes the other CTAs' released writes visible.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 // hint: bring the line holding p into L2 (no register result, never faults on a valid address)
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

@@ -7,7 +7,10 @@
 // scan permute-fusion local-experts sum array sizing"): slot[t][r] is the
 // number of earlier tokens that also go to rank r.
 //
-// One launch, one tile of 256 tokens per CTA (thread = token):
+// One launch; a tile of 256 tokens (thread = token) is handled by 1, 2, 4 or 8 CTAs
+// ("parts"), each computing the whole tile's masks and prefix and writing the rows of
+// its own share of the tile's 32-token warp groups, so that small batches spread their
+// row stores over many SMs:
 //   1. each thread reads its token's k expert ids, bumps a shared-memory expert
 //      histogram and forms its rank bit mask (R <= 256: four 64-bit words);
 //   2. a warp-level bit-matrix transpose gives, per rank, the 32-token membership
@@ -15,15 +18,17 @@
 //   3. the tile's per-rank counts are scanned across tiles with a decoupled
 //      look-back: every (tile, rank) publishes one 64-bit word holding
 //      {epoch, state, count}; state 1 = this tile's count only, state 2 = the
-//      inclusive prefix. Tiles are numbered by an atomic ticket, so a tile waits
-//      only on tiles whose CTAs already run; every wait is bounded in time and
-//      raises EP_FLAG_TIMEOUT when it gives up;
-//   4. the tile writes is_token_in_rank / slot / is_token_in_node rows with
-//      lanes across ranks (coalesced);
-//   5. expert and node counts are accumulated with atomics in the workspace;
-//      the last CTA to finish moves them to the outputs, zeroes the
-//      accumulators and the counters and advances the epoch, so the workspace
-//      is ready for the next call without a memset.
+//      inclusive prefix; part 0 publishes, every part reads. CTA i * parts + p is
+//      part p of tile i: CTAs are dispatched in index order, so a tile waits only on
+//      tiles whose CTAs already run (the order single-pass scans rely on); every
+//      wait is bounded in time and raises EP_FLAG_TIMEOUT when it gives up;
+//   4. each part writes its warp groups' rows of is_token_in_rank / slot /
+//      is_token_in_node as 16-byte vectors (the rows are contiguous);
+//   5. expert and node counts are accumulated with atomics in the workspace and
+//      each CTA then bumps a counter (release); the CTA that bumps it last moves
+//      the counts to the outputs, zeroes the accumulators and the counter and
+//      advances the epoch, so the workspace is ready for the next call without a
+//      memset. Nothing but that last CTA waits on the counter.
 #include <mutex>
 
 #include "ep_common.cuh"
@@ -39,13 +44,15 @@ constexpr int kMaxExperts = 8192;
 constexpr int kMaxTopk = 32;
 constexpr uint32_t kStateAggregate = 1u;
 constexpr uint32_t kStatePrefix = 2u;
-constexpr int kLookbackBatch = 8;
+constexpr int kLookbackBatch = 16;
+constexpr int kIdsPerPass = 8;  // expert ids a thread holds in registers at once
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
 constexpr uint32_t kWaitLimitIters = 1u << 24;               // hard cap on polls
 
 struct LayoutArgs {
     const int64_t* topk_idx;
     int T, k, E, R, rpn, N, epr, num_tiles;
+    int parts;  // CTAs per tile (1, 2, 4 or 8); CTA (tile, part) writes warp groups part*8/parts ...
     int32_t* tokens_per_expert;
     int32_t* tokens_per_rank;
     int32_t* tokens_per_node;
@@ -86,61 +93,69 @@ __device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
     return x;
 }
 
+// Polls a tile word until it carries this call's epoch and a published state; returns
+// it, or 0 (no valid word has epoch 0) once the wait has run for kWaitLimitNs or
+// kWaitLimitIters polls. Kept out of line: it runs only when a word is not ready yet.
+__device__ __noinline__ unsigned long long wait_word(const unsigned long long* p, uint32_t epoch) {
+    const unsigned long long start = globaltimer_ns();
+    for (uint32_t polls = 1; polls < kWaitLimitIters; ++polls) {
+        if (polls > 16) __nanosleep(256);
+        const unsigned long long w = ld_relaxed_u64(p);
+        if (word_epoch(w) == epoch && word_state(w) != 0u) return w;
+        if (globaltimer_ns() - start > kWaitLimitNs) break;
+    }
+    return 0ull;
+}
+
 __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
     extern __shared__ int32_t s_hist[];  // [E]
     __shared__ uint32_t s_mask[kTileWarps][kMaxRanks];
     __shared__ int32_t s_wpref[kTileWarps][kMaxRanks];
     __shared__ uint32_t s_nmask[kTileWarps][kMaxRanks];
-    __shared__ int32_t s_tile_prefix[kMaxRanks];
-    __shared__ uint32_t s_tile, s_epoch, s_stall, s_last;
+    __shared__ uint32_t s_epoch, s_stall, s_done;
 
     const int tid = static_cast<int>(threadIdx.x);
     const int lane = tid & 31;
     const int warp = tid >> 5;
+    const int tile = static_cast<int>(blockIdx.x) / a.parts;
+    const int part = static_cast<int>(blockIdx.x) - tile * a.parts;
+    const int wpp = kTileWarps / a.parts;  // warp groups this CTA writes: [w0, w0 + wpp)
+    const int w0 = part * wpp;
+    const bool own = warp >= w0 && warp < w0 + wpp;
+    const int t0 = tile * kTileTokens;
+    const int t = t0 + tid;
+    const long long* row = reinterpret_cast<const long long*>(a.topk_idx) + static_cast<size_t>(t < a.T ? t : 0) * a.k;
 
+    // the token's first expert ids are requested before anything else waits
+    long long ev[kIdsPerPass];
+#pragma unroll
+    for (int i = 0; i < kIdsPerPass; ++i) ev[i] = (t < a.T && i < a.k) ? __ldg(row + i) : -1ll;
     if (tid == 0) {
-        s_tile = atomicAdd(&a.hdr->ticket, 1u);
         s_epoch = ld_relaxed_u32(&a.hdr->epoch) + 1u;
         s_stall = ld_relaxed_u32(&a.hdr->stall_tile);
     }
-    {
-        // tiles are handed out roughly in launch order: warm L2 with this CTA's likely
-        // router rows while the ticket is on its way
-        const int tg = static_cast<int>(blockIdx.x) * kTileTokens + tid;
-        if (tg < a.T) {
-            const int64_t* row = a.topk_idx + static_cast<size_t>(tg) * a.k;
-            prefetch_l2(row);
-            prefetch_l2(row + a.k - 1);
-        }
-    }
     for (int e = tid; e < a.E; e += kTileTokens) s_hist[e] = 0;
     __syncthreads();
-
-    if (s_tile >= static_cast<uint32_t>(a.num_tiles)) {
-        // the workspace was not at rest (not zero-filled, or shared by concurrent
-        // calls): touch nothing, report it; the caller zero-fills it again
-        if (tid == 0) raise_flag(a.status, EP_FLAG_WORKSPACE);
-        return;
-    }
-    const int tile = static_cast<int>(s_tile);
     const uint32_t epoch = s_epoch;
     const bool stalled = s_stall == static_cast<uint32_t>(tile) + 1u;
-    const int t0 = tile * kTileTokens;
-    const int t = t0 + tid;
 
-    // 1. token -> rank mask, expert histogram
+    // 1. token -> rank mask; expert histogram of this CTA's own warp groups
     uint64_t m0 = 0, m1 = 0, m2 = 0, m3 = 0;
-    if (t < a.T) {
-        const int64_t* row = a.topk_idx + static_cast<size_t>(t) * a.k;
-        bool bad = false;
-        for (int j = 0; j < a.k; ++j) {
-            const int64_t e = row[j];
+    bool bad = false;
+    for (int j0 = 0; j0 < a.k; j0 += kIdsPerPass) {
+        if (j0 > 0) {
+#pragma unroll
+            for (int i = 0; i < kIdsPerPass; ++i) ev[i] = (t < a.T && j0 + i < a.k) ? __ldg(row + j0 + i) : -1ll;
+        }
+#pragma unroll
+        for (int i = 0; i < kIdsPerPass; ++i) {
+            const long long e = ev[i];
             if (e < 0) continue;
             if (e >= a.E) {
                 bad = true;
                 continue;
             }
-            atomicAdd(&s_hist[e], 1);
+            if (own) atomicAdd(&s_hist[e], 1);
             const int r = static_cast<int>(e) / a.epr;
             const uint64_t bit = 1ull << (r & 63);
             if (r < 64) m0 |= bit;
@@ -148,8 +163,8 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
             else if (r < 192) m2 |= bit;
             else m3 |= bit;
         }
-        if (bad) raise_flag(a.status, EP_FLAG_BAD_EXPERT);
     }
+    if (bad && own) raise_flag(a.status, EP_FLAG_BAD_EXPERT);
 
     // 2. per-rank warp membership masks: for each chunk of 32 ranks, the warp holds a
     //    32 x 32 bit matrix (lane = token, bit = rank); transposing it leaves in lane j
@@ -161,34 +176,44 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
     }
     __syncthreads();
 
-    // expert and node counts of this tile -> workspace accumulators
+    // 3. the tile's per-rank counts; part 0 publishes them first (later tiles wait on them)
+    uint32_t agg = 0;
+    if (tid < a.R) {
+        int run = 0;
+        for (int w = 0; w < kTileWarps; ++w) {
+            s_wpref[w][tid] = run;
+            run += __popc(s_mask[w][tid]);
+        }
+        agg = static_cast<uint32_t>(run);
+        if (part == 0 && !stalled)
+            st_relaxed_u64(a.words + static_cast<size_t>(tile) * a.R + tid,
+                           pack_word(epoch, tile == 0 ? kStatePrefix : kStateAggregate, agg));
+    }
+    // expert and node counts of the own warp groups -> workspace accumulators; the node
+    // masks are formed by the highest threads, which take no part in the look-back when
+    // R is small
     for (int e = tid; e < a.E; e += kTileTokens) {
         const int c = s_hist[e];
         if (c != 0) atomicAdd(&a.acc_expert[e], c);
     }
-    for (int n = tid; n < a.N; n += kTileTokens) {
-        int c = 0;
-        for (int w = 0; w < kTileWarps; ++w) {
-            uint32_t m = 0;
-            for (int q = 0; q < a.rpn; ++q) m |= s_mask[w][n * a.rpn + q];
-            s_nmask[w][n] = m;
-            c += __popc(m);
+    {
+        const int n = kTileTokens - 1 - tid;
+        if (n < a.N) {
+            int c = 0;
+            for (int w = w0; w < w0 + wpp; ++w) {
+                uint32_t m = 0;
+                for (int q = 0; q < a.rpn; ++q) m |= s_mask[w][n * a.rpn + q];
+                s_nmask[w][n] = m;
+                c += __popc(m);
+            }
+            if (c != 0) atomicAdd(&a.acc_node[n], c);
         }
-        if (c != 0) atomicAdd(&a.acc_node[n], c);
     }
 
-    // 3. per-rank scan across tiles (decoupled look-back), thread r owns rank r
+    // per-rank scan across tiles (decoupled look-back), thread r owns rank r; every part
+    // of the tile reads the same words, part 0 alone publishes the inclusive prefix
     if (tid < a.R) {
         const int r = tid;
-        int run = 0;
-        for (int w = 0; w < kTileWarps; ++w) {
-            s_wpref[w][r] = run;
-            run += __popc(s_mask[w][r]);
-        }
-        const uint32_t agg = static_cast<uint32_t>(run);
-        unsigned long long* my_word = a.words + static_cast<size_t>(tile) * a.R + r;
-        if (!stalled) st_relaxed_u64(my_word, pack_word(epoch, tile == 0 ? kStatePrefix : kStateAggregate, agg));
-
         uint32_t excl = 0;
         bool timed_out = false;
         int j = tile - 1;
@@ -202,20 +227,13 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
 #pragma unroll
             for (int i = 0; i < kLookbackBatch; ++i) {
                 if (i >= nb || found_prefix || timed_out) continue;
-                const unsigned long long* p = a.words + static_cast<size_t>(j - i) * a.R + r;
                 unsigned long long w = wv[i];
                 if (word_epoch(w) != epoch || word_state(w) == 0u) {
-                    const unsigned long long start = globaltimer_ns();
-                    uint32_t polls = 0;
-                    while (word_epoch(w) != epoch || word_state(w) == 0u) {
-                        if (++polls >= kWaitLimitIters || globaltimer_ns() - start > kWaitLimitNs) {
-                            timed_out = true;
-                            break;
-                        }
-                        if (polls > 16) __nanosleep(256);
-                        w = ld_relaxed_u64(p);
+                    w = wait_word(a.words + static_cast<size_t>(j - i) * a.R + r, epoch);
+                    if (w == 0ull) {
+                        timed_out = true;
+                        continue;
                     }
-                    if (timed_out) break;
                 }
                 excl += word_value(w);
                 if (word_state(w) == kStatePrefix) found_prefix = true;
@@ -224,61 +242,115 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
             j -= nb;
         }
         if (timed_out) raise_flag(a.status, EP_FLAG_TIMEOUT);
-        if (tile > 0 && !stalled) st_relaxed_u64(my_word, pack_word(epoch, kStatePrefix, excl + agg));
-        s_tile_prefix[r] = static_cast<int32_t>(excl);
-        if (tile == a.num_tiles - 1) a.tokens_per_rank[r] = static_cast<int32_t>(excl + agg);
+        if (part == 0 && tile > 0 && !stalled)
+            st_relaxed_u64(a.words + static_cast<size_t>(tile) * a.R + r, pack_word(epoch, kStatePrefix, excl + agg));
+        for (int w = w0; w < w0 + wpp; ++w) s_wpref[w][r] += static_cast<int32_t>(excl);
+        if (part == 0 && tile == a.num_tiles - 1) a.tokens_per_rank[r] = static_cast<int32_t>(excl + agg);
     }
     __syncthreads();
 
-    // 4. rows of is_token_in_rank / slot / is_token_in_node. Warp w writes the 32
-    //    tokens of its own ballot group: per rank it reads the group's mask word and
-    //    prefixes once, then emits 32 independent (in_rank, slot) pairs, lanes across
-    //    ranks so that each store instruction covers consecutive ranks of one token.
+    // this CTA's accumulator contributions are in (the barrier above orders every
+    // thread's atomics before the release); the answer is needed only at the end
+    uint32_t done_before = 0;
+    if (tid == kTileTokens - 1) done_before = atom_add_acq_rel_u32(&a.hdr->done, 1u);
+
+    // 4. rows of is_token_in_rank / slot / is_token_in_node of the own warp groups: one
+    //    contiguous run per array (the groups start at token t0 + 32 * w0), written as
+    //    16-byte vectors, consecutive threads on consecutive vectors; entry f of the run
+    //    is (token f / width, column f % width). The bytes past the last whole vector
+    //    (only at the end of the batch) are written one by one.
     {
-        const int g0 = warp * 32;  // first tile-local token of this warp's group
-        const int ng = a.T - t0 - g0 < 32 ? a.T - t0 - g0 : 32;
-        for (int r = lane; r < a.R && ng > 0; r += 32) {
-            const uint32_t m = s_mask[warp][r];
-            const int32_t base_slot = s_tile_prefix[r] + s_wpref[warp][r];
-            uint8_t* ir = a.in_rank + static_cast<size_t>(t0 + g0) * a.R + r;
-            int32_t* sl = a.slot + static_cast<size_t>(t0 + g0) * a.R + r;
-            int before = 0;  // group tokens before u that go to rank r
-#pragma unroll 8
-            for (int u = 0; u < 32; ++u) {
-                if (u < ng) {
-                    const bool in = (m >> u) & 1u;
-                    ir[static_cast<size_t>(u) * a.R] = in ? 1 : 0;
-                    sl[static_cast<size_t>(u) * a.R] = in ? base_slot + before : -1;
-                    before += in ? 1 : 0;
+        const int first = t0 + 32 * w0;
+        const int ntok = a.T - first < 32 * wpp ? a.T - first : 32 * wpp;
+        if (ntok > 0) {
+            // slot: 4 entries per vector; s_wpref holds the rank's slot of the first
+            // token of each own warp group
+            {
+                int32_t* base = a.slot + static_cast<size_t>(first) * a.R;
+                const int ne = ntok * a.R;
+                for (int c = tid; c < ne / 4; c += kTileTokens) {
+                    int u = (4 * c) / a.R;
+                    int r = 4 * c - u * a.R;
+                    int32_t v[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int w = w0 + (u >> 5);
+                        const uint32_t m = s_mask[w][r];
+                        const uint32_t b = 1u << (u & 31);
+                        v[q] = (m & b) ? s_wpref[w][r] + __popc(m & (b - 1u)) : -1;
+                        if (++r == a.R) {
+                            r = 0;
+                            ++u;
+                        }
+                    }
+                    st_v4(base + 4 * c, make_uint4(static_cast<uint32_t>(v[0]), static_cast<uint32_t>(v[1]),
+                                                   static_cast<uint32_t>(v[2]), static_cast<uint32_t>(v[3])));
+                }
+                for (int f = (ne & ~3) + tid; f < ne; f += kTileTokens) {
+                    const int u = f / a.R, r = f - (f / a.R) * a.R;
+                    const int w = w0 + (u >> 5);
+                    const uint32_t m = s_mask[w][r];
+                    const uint32_t b = 1u << (u & 31);
+                    base[f] = (m & b) ? s_wpref[w][r] + __popc(m & (b - 1u)) : -1;
                 }
             }
-        }
-        if (a.in_node != nullptr) {
-            for (int n = lane; n < a.N && ng > 0; n += 32) {
-                const uint32_t m = s_nmask[warp][n];
-                uint8_t* in = a.in_node + static_cast<size_t>(t0 + g0) * a.N + n;
-#pragma unroll 8
-                for (int u = 0; u < 32; ++u)
-                    if (u < ng) in[static_cast<size_t>(u) * a.N] = (m >> u) & 1u;
-            }
+            // membership bytes of one mask table, 16 entries per vector
+            auto write_bits = [&](uint8_t* base, const uint32_t (*mask)[kMaxRanks], int width) {
+                const int nb = ntok * width;
+                for (int c = tid; c < nb / 16; c += kTileTokens) {
+                    int u = (16 * c) / width;
+                    int r = 16 * c - u * width;
+                    uint32_t wd[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        wd[q >> 2] |= ((mask[w0 + (u >> 5)][r] >> (u & 31)) & 1u) << (8 * (q & 3));
+                        if (++r == width) {
+                            r = 0;
+                            ++u;
+                        }
+                    }
+                    st_v4(base + 16 * c, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+                }
+                for (int f = (nb & ~15) + tid; f < nb; f += kTileTokens) {
+                    const int u = f / width, r = f - (f / width) * width;
+                    base[f] = static_cast<uint8_t>((mask[w0 + (u >> 5)][r] >> (u & 31)) & 1u);
+                }
+            };
+            write_bits(a.in_rank + static_cast<size_t>(first) * a.R, s_mask, a.R);
+            if (a.in_node != nullptr) write_bits(a.in_node + static_cast<size_t>(first) * a.N, s_nmask, a.N);
         }
     }
 
-    // 5. last CTA: move the accumulated counts out and reset the workspace
-    __threadfence();
+    // 5. the CTA that finishes the count last moves the accumulated counts out and
+    //    resets the workspace (every CTA read the epoch before it counted itself)
+    if (tid == kTileTokens - 1) s_done = done_before;
     __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&a.hdr->done, 1u) == static_cast<uint32_t>(a.num_tiles - 1);
-    __syncthreads();
-    if (s_last) {
-        __threadfence();
+    const uint32_t done = s_done;
+    const uint32_t ctas = static_cast<uint32_t>(a.num_tiles * a.parts);
+    if (done >= ctas) {
+        // the workspace was not at rest (not zero-filled, or shared by concurrent
+        // calls): report it; the caller zero-fills it again
+        if (tid == 0) raise_flag(a.status, EP_FLAG_WORKSPACE);
+    } else if (done == ctas - 1u) {
+        // the counter's acquire (thread 255) and the barrier above order the other
+        // CTAs' accumulator atomics before these reads
         for (int e = tid; e < a.E; e += kTileTokens) a.tokens_per_expert[e] = atomicExch(&a.acc_expert[e], 0);
         for (int n = tid; n < a.N; n += kTileTokens) a.tokens_per_node[n] = atomicExch(&a.acc_node[n], 0);
         if (tid == 0) {
-            atomicExch(&a.hdr->ticket, 0u);
             atomicExch(&a.hdr->done, 0u);
             atomicExch(&a.hdr->epoch, epoch);
         }
     }
+}
+
+// CTAs per tile: the largest power of two (at most one CTA per warp group) that keeps
+// the grid within one CTA per SM, so that the batch's row stores spread over most SMs
+// (one SM issues scattered row stores at only a few tens of GB/s).
+int parts_for(int num_tiles) {
+    const long long sms = sm_count();
+    int parts = 1;
+    while (parts < kTileWarps && static_cast<long long>(num_tiles) * (2 * parts) <= sms) parts *= 2;
+    return parts;
 }
 
 bool g_smem_attr_set[64] = {};
@@ -354,7 +426,8 @@ extern "C" ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t
         if (err != cudaSuccess) return cuda_fail(err);
         g_smem_attr_set[dev] = true;
     }
-    layout_kernel<<<a.num_tiles, kTileTokens, smem, as_stream(stream)>>>(a);
+    a.parts = parts_for(a.num_tiles);
+    layout_kernel<<<a.num_tiles * a.parts, kTileTokens, smem, as_stream(stream)>>>(a);
     return check_launch();
 }
 
@@ -460,6 +533,7 @@ extern "C" ep_status_t ep_get_layout_noalloc(const int64_t* topk_idx, int32_t T,
         if (err != cudaSuccess) return cuda_fail(err);
         g_smem_attr_set[dev] = true;
     }
-    layout_kernel<<<a.num_tiles, kTileTokens, static_cast<size_t>(E) * sizeof(int32_t), as_stream(stream)>>>(a);
+    a.parts = parts_for(a.num_tiles);
+    layout_kernel<<<a.num_tiles * a.parts, kTileTokens, static_cast<size_t>(E) * sizeof(int32_t), as_stream(stream)>>>(a);
     return check_launch();
 }

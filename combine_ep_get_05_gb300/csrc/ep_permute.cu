@@ -58,69 +58,75 @@ struct ExpertLayoutArgs {
     int32_t* status;
 };
 
-// expert of (t, j) if it counts (in range and the first occurrence in the row), else -1
-__device__ __forceinline__ int entry_expert(const int64_t* row, int j, int E, bool& bad) {
-    const int64_t e = row[j];
-    if (e < 0) return -1;
-    if (e >= E) {
-        bad = true;
-        return -1;
-    }
-    for (int jj = 0; jj < j; ++jj)
-        if (row[jj] == e) {
-            bad = true;
-            return -1;
-        }
-    return static_cast<int>(e);
-}
-
-// One tile of 256 tokens per CTA (thread = token). Each warp builds, per expert, the
-// 32-bit mask of its tokens that chose the expert (shared-memory atomic ORs: the result
-// does not depend on their order); a token's rank among the warp's tokens with the same
-// expert is the popcount of the mask below its lane. Per-expert tile counts are scanned
-// across tiles by a decoupled look-back over epoch-tagged words (bounded waits); the tile
-// holding the last tokens, which ends up with every expert's total, writes the offsets.
+// One tile of 256 tokens per CTA (thread = token); tile i is CTA i (CTAs are dispatched
+// in index order, so a tile waits only on tiles whose CTAs already run). Each thread reads
+// its token's ids (eight loads in flight at a time) and keeps, per top-k slot, the expert
+// the entry counts for (in range and the first occurrence in the row) or -1, in shared
+// memory. Each warp builds, per expert, the 32-bit mask of its tokens that chose the
+// expert (shared-memory atomic ORs: the result does not depend on their order); a
+// token's rank among the warp's tokens with the same expert is the popcount of the mask
+// below its lane. Per-expert tile counts are scanned across tiles by a decoupled
+// look-back over epoch-tagged words (bounded waits); the tile holding the last tokens,
+// which ends up with every expert's total, writes the offsets.
 __global__ void __launch_bounds__(kThreads, 2) expert_layout_kernel(ExpertLayoutArgs a) {
     extern __shared__ uint32_t smem[];
     uint32_t* s_emask = smem;                                              // [kWarps][E]
     int32_t* s_wpref = reinterpret_cast<int32_t*>(smem + kWarps * a.E);  // [kWarps][E]
     int32_t* s_tpref = s_wpref + kWarps * a.E;                           // [E]
     int32_t* s_total = s_tpref + a.E;                                    // [E]
-    __shared__ uint32_t s_tile, s_epoch, s_stall, s_last;
+    int32_t* s_ex = s_total + a.E;                                       // [k][kThreads]
+    __shared__ uint32_t s_epoch, s_stall, s_done;
     __shared__ int32_t s_part[kThreads];
 
     const int tid = static_cast<int>(threadIdx.x);
     const int lane = tid & 31;
     const int warp = tid >> 5;
+    const int tile = static_cast<int>(blockIdx.x);
+    const int t = tile * kThreads + tid;
+    const long long* row = reinterpret_cast<const long long*>(a.topk_idx) + static_cast<size_t>(t < a.T ? t : 0) * a.k;
+
+    long long ev[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) ev[i] = (t < a.T && i < a.k) ? __ldg(row + i) : -1ll;
     if (tid == 0) {
-        s_tile = atomicAdd(&a.hdr->ticket, 1u);
         s_epoch = ld_relaxed_u32(&a.hdr->epoch) + 1u;
         s_stall = ld_relaxed_u32(&a.hdr->stall_tile);
     }
-    {
-        const int tg = static_cast<int>(blockIdx.x) * kThreads + tid;
-        if (tg < a.T) prefetch_l2(a.topk_idx + static_cast<size_t>(tg) * a.k);
-    }
     for (int e = lane; e < a.E; e += 32) s_emask[warp * a.E + e] = 0u;
     __syncthreads();
-    if (s_tile >= static_cast<uint32_t>(a.num_tiles)) {
-        if (tid == 0) raise_flag(a.status, EP_FLAG_WORKSPACE);
-        return;
-    }
-    const int tile = static_cast<int>(s_tile);
     const uint32_t epoch = s_epoch;
     const bool stalled = s_stall == static_cast<uint32_t>(tile) + 1u;
-    const int t = tile * kThreads + tid;
-    const int64_t* row = a.topk_idx + static_cast<size_t>(t < a.T ? t : 0) * a.k;
 
-    if (t < a.T) {
-        bool bad = false;
-        for (int j = 0; j < a.k; ++j) {
-            const int e = entry_expert(row, j, a.E, bad);
-            if (e >= 0) atomicOr(&s_emask[warp * a.E + e], 1u << lane);
+    bool bad = false;
+    for (int j0 = 0; j0 < a.k; j0 += kBatch) {
+        if (j0 > 0) {
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) ev[i] = (t < a.T && j0 + i < a.k) ? __ldg(row + j0 + i) : -1ll;
         }
-        if (bad) raise_flag(a.status, EP_FLAG_BAD_EXPERT);
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int j = j0 + i;
+            if (j >= a.k) break;
+            const long long e = ev[i];
+            int x = -1;
+            if (t < a.T && e >= 0) {
+                if (e >= a.E) {
+                    bad = true;
+                } else {
+                    // a repeat of an earlier slot of the row counts once
+                    bool rep = false;
+#pragma unroll
+                    for (int ii = 0; ii < i; ++ii) rep |= ev[ii] == e;
+                    for (int jj = 0; jj < j0; ++jj) rep |= s_ex[jj * kThreads + tid] == static_cast<int>(e);
+                    if (rep) bad = true;
+                    else x = static_cast<int>(e);
+                }
+            }
+            s_ex[j * kThreads + tid] = x;
+            if (x >= 0) atomicOr(&s_emask[warp * a.E + x], 1u << lane);
+        }
     }
+    if (bad) raise_flag(a.status, EP_FLAG_BAD_EXPERT);
     __syncthreads();
 
     for (int e = tid; e < a.E; e += kThreads) {
@@ -173,6 +179,10 @@ __global__ void __launch_bounds__(kThreads, 2) expert_layout_kernel(ExpertLayout
     }
     __syncthreads();
 
+    // every CTA read the epoch before it counts itself here; the last one resets
+    uint32_t done_before = 0;
+    if (tid == kThreads - 1) done_before = atom_add_acq_rel_u32(&a.hdr->done, 1u);
+
     // the tile with the last tokens knows every expert's total: write the offsets
     if (tile == a.num_tiles - 1) {
         const int per = (a.E + kThreads - 1) / kThreads;
@@ -203,24 +213,20 @@ __global__ void __launch_bounds__(kThreads, 2) expert_layout_kernel(ExpertLayout
 
     if (t < a.T) {
         const uint32_t below = (1u << lane) - 1u;
-        bool bad = false;
         for (int j = 0; j < a.k; ++j) {
-            const int e = entry_expert(row, j, a.E, bad);
+            const int e = s_ex[j * kThreads + tid];
             int32_t v = -1;
-            if (e >= 0)
-                v = s_tpref[e] + s_wpref[warp * a.E + e] + __popc(s_emask[warp * a.E + e] & below);
+            if (e >= 0) v = s_tpref[e] + s_wpref[warp * a.E + e] + __popc(s_emask[warp * a.E + e] & below);
             a.eslot[static_cast<size_t>(t) * a.k + j] = v;
         }
     }
 
-    // last CTA to finish resets the ticket and advances the epoch
-    __threadfence();
+    if (tid == kThreads - 1) s_done = done_before;
     __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&a.hdr->done, 1u) == static_cast<uint32_t>(a.num_tiles - 1);
-    __syncthreads();
-    if (s_last && tid == 0) {
-        __threadfence();
-        atomicExch(&a.hdr->ticket, 0u);
+    const uint32_t done = s_done;
+    if (done >= static_cast<uint32_t>(a.num_tiles)) {
+        if (tid == 0) raise_flag(a.status, EP_FLAG_WORKSPACE);
+    } else if (done == static_cast<uint32_t>(a.num_tiles - 1) && tid == 0) {
         atomicExch(&a.hdr->done, 0u);
         atomicExch(&a.hdr->epoch, epoch);
     }
@@ -574,12 +580,13 @@ extern "C" ep_status_t ep_get_expert_layout(const int64_t* topk_idx, int32_t T, 
     a.hdr = static_cast<ep_layout_ws_header_t*>(workspace);
     a.words = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + 256);
     a.status = status;
-    const size_t smem = static_cast<size_t>(E) * (2 * kWarps + 2) * sizeof(int32_t);
+    const size_t smem = (static_cast<size_t>(E) * (2 * kWarps + 2) + static_cast<size_t>(k) * kThreads) * sizeof(int32_t);
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
         cudaError_t err = cudaFuncSetAttribute(expert_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kMaxExpertsPerm * (2 * kWarps + 2) * static_cast<int>(sizeof(int32_t)));
+                                               (kMaxExpertsPerm * (2 * kWarps + 2) + kMaxTopk * kThreads) *
+                                                   static_cast<int>(sizeof(int32_t)));
         if (err != cudaSuccess) return cuda_fail(err);
         g_attr_set[dev] = true;
     }

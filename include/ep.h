@@ -87,12 +87,12 @@ size_t ep_layout_workspace_size(int32_t T, int32_t E, int32_t R, int32_t ranks_p
 
 /* First bytes of the layout workspace. The workspace must be zero-filled once
  * before its first use; every completed call leaves it ready for the next call
- * (the counters return to zero and the epoch advances). `stall_tile` is a test
+ * (the counter returns to zero and the epoch advances). `stall_tile` is a test
  * hook: when it holds i + 1, tile i never publishes its counts, so that the
  * bounded waits of its successors run out and raise EP_FLAG_TIMEOUT. Keep it 0. */
 typedef struct {
-    uint32_t ticket;     /* next tile index handed out */
-    uint32_t done;       /* tiles finished */
+    uint32_t reserved;   /* unused, left as found */
+    uint32_t done;       /* tiles that have added their counts */
     uint32_t epoch;      /* calls completed on this workspace */
     uint32_t stall_tile; /* test hook, 0 = off */
 } ep_layout_ws_header_t;

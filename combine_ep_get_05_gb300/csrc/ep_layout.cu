@@ -210,6 +210,13 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
         }
     }
 
+    // this CTA's accumulator contributions are issued: the barrier orders every thread's
+    // atomics before the release of the counter, which the last warp takes (off the
+    // look-back's warps when R is small); the answer is needed only after the scan
+    __syncthreads();
+    uint32_t done_before = 0;
+    if (tid == kTileTokens - 1) done_before = atom_add_acq_rel_u32(&a.hdr->done, 1u);
+
     // per-rank scan across tiles (decoupled look-back), thread r owns rank r; every part
     // of the tile reads the same words, part 0 alone publishes the inclusive prefix
     if (tid < a.R) {
@@ -247,12 +254,10 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
         for (int w = w0; w < w0 + wpp; ++w) s_wpref[w][r] += static_cast<int32_t>(excl);
         if (part == 0 && tile == a.num_tiles - 1) a.tokens_per_rank[r] = static_cast<int32_t>(excl + agg);
     }
+    if (tid == kTileTokens - 1) s_done = done_before;
     __syncthreads();
-
-    // this CTA's accumulator contributions are in (the barrier above orders every
-    // thread's atomics before the release); the answer is needed only at the end
-    uint32_t done_before = 0;
-    if (tid == kTileTokens - 1) done_before = atom_add_acq_rel_u32(&a.hdr->done, 1u);
+    const uint32_t done = s_done;
+    const uint32_t ctas = static_cast<uint32_t>(a.num_tiles * a.parts);
 
     // 4. rows of is_token_in_rank / slot / is_token_in_node of the own warp groups: one
     //    contiguous run per array (the groups start at token t0 + 32 * w0), written as
@@ -321,19 +326,15 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
         }
     }
 
-    // 5. the CTA that finishes the count last moves the accumulated counts out and
-    //    resets the workspace (every CTA read the epoch before it counted itself)
-    if (tid == kTileTokens - 1) s_done = done_before;
-    __syncthreads();
-    const uint32_t done = s_done;
-    const uint32_t ctas = static_cast<uint32_t>(a.num_tiles * a.parts);
+    // 5. the CTA that counted itself last moves the accumulated counts out and resets
+    //    the workspace (every CTA read the epoch before it counted itself)
     if (done >= ctas) {
         // the workspace was not at rest (not zero-filled, or shared by concurrent
         // calls): report it; the caller zero-fills it again
         if (tid == 0) raise_flag(a.status, EP_FLAG_WORKSPACE);
     } else if (done == ctas - 1u) {
-        // the counter's acquire (thread 255) and the barrier above order the other
-        // CTAs' accumulator atomics before these reads
+        // the counter's acquire (last thread) and the barrier after the scan order the
+        // other CTAs' accumulator atomics before these reads
         for (int e = tid; e < a.E; e += kTileTokens) a.tokens_per_expert[e] = atomicExch(&a.acc_expert[e], 0);
         for (int n = tid; n < a.N; n += kTileTokens) a.tokens_per_node[n] = atomicExch(&a.acc_node[n], 0);
         if (tid == 0) {

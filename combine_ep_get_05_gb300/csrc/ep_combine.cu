@@ -40,6 +40,7 @@ __device__ __forceinline__ void add8(float* acc, const uint4& v) {
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ slot, int T, int H, int R,
                    int max_tokens, uint16_t* __restrict__ out, int32_t* status) {
+    ep::grid_dependency_wait();  // dependent launch: the slabs are complete after this
     __shared__ long long s_src[kWarps][kMaxSrc];
     const int lane = ep::lane_id();
     const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -116,7 +117,7 @@ extern "C" ep_status_t ep_combine(const void* y, const int32_t* slot, int32_t T,
     const long long want = (items + kWarps - 1) / kWarps;
     const long long cap = static_cast<long long>(sm_count()) * per_sm;
     const int grid = static_cast<int>(want < cap ? want : cap);
-    combine_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(static_cast<const uint16_t*>(y), slot, T, H, R,
-                                                             max_tokens, static_cast<uint16_t*>(out), status);
-    return check_launch();
+    return launch_dependent(combine_kernel, dim3(grid), dim3(kThreads), 0, as_stream(stream),
+                            static_cast<const uint16_t*>(y), slot, T, H, R, max_tokens, static_cast<uint16_t*>(out),
+                            status);
 }

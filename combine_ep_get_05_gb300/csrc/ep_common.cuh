@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "ep.h"
 
@@ -27,6 +28,29 @@ ep_status_t check_launch();
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned16_or_null(const void* p) { return p == nullptr || aligned16(p); }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Launch kernel<<<grid, block, smem, stream>>>(args...) as a programmatic dependent launch:
+// it may be scheduled before the previous kernel of the stream has ended, once every CTA
+// of that kernel has called allow_dependents() (or ended), so its CTAs are resident and
+// set up when the data arrives. The kernel must call grid_dependency_wait() before it
+// reads global memory: that wait returns once the previous kernel has completed and its
+// writes are visible. Returns EP_OK or EP_ERR_CUDA.
+template <typename... KArgs, typename... Args>
+ep_status_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return err == cudaSuccess ? check_launch() : cuda_fail(err);
+}
 
 // ---------------------------------------------------------------- device side
 
@@ -83,6 +107,12 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+// Programmatic dependent launch, device side: wait until the previous kernel of the
+// stream has completed and its writes are visible (returns at once for an ordinary
+// launch); and allow the next kernel, if launched with launch_dependent, to be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // hint: bring the line holding p into L2 (no register result, never faults on a valid address)
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

@@ -94,6 +94,7 @@ __device__ __forceinline__ void write_metadata(const DispatchArgs& a, int t, int
 }
 
 __global__ void __launch_bounds__(kThreads, 2) dispatch_bf16_kernel(DispatchArgs a) {
+    ep::grid_dependency_wait();  // dependent launch: inputs are ready after this
     __shared__ int s_rank[kWarps][kMaxDest];
     __shared__ long long s_row[kWarps][kMaxDest];
     const int lane = ep::lane_id();
@@ -222,6 +223,7 @@ __device__ __forceinline__ void quantize16(const uint4& a, const uint4& b, uint4
 // vector per lane (512 bytes per warp instruction) and the 4 scales of an
 // iteration leave in one 16-byte store when they are 16-byte aligned.
 __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a, int interleave) {
+    ep::grid_dependency_wait();  // dependent launch: inputs are ready after this
     __shared__ int s_rank[kWarps][kMaxDest];
     __shared__ long long s_row[kWarps][kMaxDest];
     const int lane = ep::lane_id();
@@ -347,12 +349,11 @@ extern "C" ep_status_t ep_dispatch(const void* x, ep_dtype_t out_dtype, const in
         const long long resident = static_cast<long long>(sm_count()) * per_sm;
         const bool one_wave = static_cast<long long>(T) <= resident * kWarps;
         const int grid = one_wave ? static_cast<int>(resident) : grid_for(T, 8);
-        dispatch_fp8_kernel<<<grid, kThreads, 0, as_stream(stream)>>>(a, one_wave ? 1 : 0);
-    } else {
-        const DispatchScatter sp{a, static_cast<char*>(recv_x), static_cast<uint32_t>(H) * 2u, status};
-        const ep_status_t st = launch_scatter_rows(sp, T, as_stream(stream));
-        if (st != EP_ERR_INVALID) return st;  // rows too large for the shared-memory buffers: registers
-        dispatch_bf16_kernel<<<grid_for(T, 8), kThreads, 0, as_stream(stream)>>>(a);
+        return launch_dependent(dispatch_fp8_kernel, dim3(grid), dim3(kThreads), 0, as_stream(stream), a,
+                                one_wave ? 1 : 0);
     }
-    return check_launch();
+    const DispatchScatter sp{a, static_cast<char*>(recv_x), static_cast<uint32_t>(H) * 2u, status};
+    const ep_status_t st = launch_scatter_rows(sp, T, as_stream(stream));
+    if (st != EP_ERR_INVALID) return st;  // rows too large for the shared-memory buffers: registers
+    return launch_dependent(dispatch_bf16_kernel, dim3(grid_for(T, 8)), dim3(kThreads), 0, as_stream(stream), a);
 }

@@ -108,6 +108,9 @@ __device__ __noinline__ unsigned long long wait_word(const unsigned long long* p
 }
 
 __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
+    // the next kernel (a dispatch launched as a dependent launch) may be scheduled now: its
+    // CTAs settle on the SMs this grid leaves free and wait there for its completion
+    allow_dependents();
     extern __shared__ int32_t s_hist[];  // [E]
     __shared__ uint32_t s_mask[kTileWarps][kMaxRanks];
     __shared__ int32_t s_wpref[kTileWarps][kMaxRanks];

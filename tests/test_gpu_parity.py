@@ -99,6 +99,9 @@ def run_rank_path(w, max_tokens=None, full_compare=True):
     ("dsv3", {"T": 777, "H": 7168}),
     ("dsv3_fp8", {"T": 1000, "H": 1024}),
     ("dsv3_fp8", {"T": 333, "H": 384}),
+    ("dsv3_fp8", {"T": 300, "H": 24576}),  # wide FP8 rows
+    ("dsv3_fp8", {"T": 40, "H": 26624}),
+    ("dsv3", {"T": 40, "H": 36864}),       # bf16 rows too large for the bulk-copy scatter
     ("skewed", {"T": 2000, "H": 256}),
     ("restripe", {"T": 700, "H": 512}),
 ])
@@ -264,6 +267,7 @@ def run_node_path(w, chunk=None, P_override=None):
     ({"T": 33, "H": 8, "P": 8, "N": 1, "ranks_per_node": 2}, 7),
     ({"T": 4097, "H": 128, "P": 128, "N": 16, "ranks_per_node": 2}, 256),
     ({"T": 600, "H": 256, "max_tokens": 1000}, 64),
+    ({"T": 40, "H": 36864, "P": 8}, 16),  # rows too large for the bulk-copy scatter
 ])
 def test_node_path_matches_oracle(over, chunk):
     run_node_path(workloads.make("restripe", **over), chunk=chunk)

@@ -106,6 +106,7 @@ def run_permuted(w, max_rows=None, weighted=True):
     ("dsv3", {"T": 777, "H": 7168}),
     ("skewed", {"T": 3000, "H": 256}),
     ("restripe", {"T": 600, "H": 128}),
+    ("dsv3", {"T": 40, "H": 36864}),  # rows too large for the bulk-copy scatter
 ])
 def test_permuted_path_matches_oracle(name, over):
     run_permuted(workloads.make(name, **over))

@@ -72,6 +72,8 @@ def _load():
                 "oracle_restripe_prob": (None, [P, i32, i32, i32, i32, P]),
                 "oracle_dispatch_nodes": (i32, [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P]),
                 "oracle_combine": (i32, [P, P, i32, i32, i32, i32, P]),
+                "oracle_combine_fp8": (i32, [P, P, P, i32, i32, i32, i32, P]),
+                "oracle_combine_weights": (i32, [P, P, i32, i32, i32, i32, P]),
                 "oracle_expert_scale": (None, [P, i32, P, P, P, i32, i32, i32, i32, P]),
                 "oracle_expert_layout": (i32, [P, i32, i32, i32, P, P]),
                 "oracle_dispatch_permuted": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]),
@@ -217,6 +219,29 @@ def combine(y_bits, slot, max_tokens: int) -> tuple:
     T = sl.shape[0]
     out = np.zeros((T, H), np.uint16)
     flags = int(_load().oracle_combine(_ptr(y), _ptr(sl), T, H, R, max_tokens, _ptr(out)))
+    return out, flags
+
+
+def combine_fp8(y_codes, y_scales, slot, max_tokens: int) -> tuple:
+    """Combine of FP8 rows: each row dequantised to fp32(e4m3(q) * scale), then as combine()."""
+    y = _c(y_codes, np.uint8)
+    sc = _c(y_scales, np.float32)
+    sl = _c(slot, np.int32)
+    R, _, H = y.shape
+    T = sl.shape[0]
+    out = np.zeros((T, H), np.uint16)
+    flags = int(_load().oracle_combine_fp8(_ptr(y), _ptr(sc), _ptr(sl), T, H, R, max_tokens, _ptr(out)))
+    return out, flags
+
+
+def combine_weights(recv_topk_w, slot, max_tokens: int) -> tuple:
+    """Combined top-k weights [T][k]: fp32 sum over ranks ascending of the received weight rows."""
+    w = _c(recv_topk_w, np.float32)
+    sl = _c(slot, np.int32)
+    R, _, k = w.shape
+    T = sl.shape[0]
+    out = np.zeros((T, k), np.float32)
+    flags = int(_load().oracle_combine_weights(_ptr(w), _ptr(sl), T, k, R, max_tokens, _ptr(out)))
     return out, flags
 
 

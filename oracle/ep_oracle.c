@@ -383,6 +383,67 @@ int32_t oracle_combine(const uint16_t* y, const int32_t* slot, int32_t T, int32_
     return flags;
 }
 
+/* Combine of FP8 expert outputs. The pages show only the BF16 combine ([PR #347]
+ * 3.2.1) and, for FP8, the dispatch row format (H E4M3 codes and one fp32 scale per
+ * 128 channels). Reading: a received FP8 row is dequantised exactly as the dispatch
+ * wrote it, v[h] = fp32(e4m3(q[h]) * scale[h / 128]) (one fp32 rounding), and reduced
+ * as oracle_combine does:
+ *   acc = 0 (fp32); for r = 0, 1, ..., R-1 with s = slot[t][r] >= 0: acc = acc + v
+ *   out[t][h] = bf16_rn(acc)
+ * Slots at or beyond max_tokens are skipped and raise ORACLE_FLAG_CAPACITY. */
+int32_t oracle_combine_fp8(const uint8_t* y, const float* y_scales, const int32_t* slot, int32_t T,
+                           int32_t H, int32_t R, int32_t max_tokens, uint16_t* out) {
+    int32_t flags = 0;
+    int32_t nb = H / 128;
+    float* acc = (float*)malloc((size_t)H * sizeof(float) + 1);
+    for (int32_t t = 0; t < T; ++t) {
+        for (int32_t h = 0; h < H; ++h) acc[h] = 0.0f;
+        for (int32_t r = 0; r < R; ++r) {
+            int32_t s = slot[(size_t)t * R + r];
+            if (s < 0) continue;
+            if (s >= max_tokens) {
+                flags |= ORACLE_FLAG_CAPACITY;
+                continue;
+            }
+            size_t yr = (size_t)r * max_tokens + s;
+            for (int32_t h = 0; h < H; ++h) {
+                float v = oracle_e4m3_to_f32(y[yr * H + h]) * y_scales[yr * nb + h / 128];
+                acc[h] = acc[h] + v;
+            }
+        }
+        for (int32_t h = 0; h < H; ++h) out[(size_t)t * H + h] = oracle_f32_to_bf16(acc[h]);
+    }
+    free(acc);
+    return flags;
+}
+
+/* Combined top-k weights: the combine also brings the received weight rows back to
+ * token order ([PR #347] 2.1: the combine returns what the dispatch sent out). Each
+ * rank's copy of a token carries w_j for the slots whose expert it holds and 0 for
+ * the others, so
+ *   out[t][j] = sum over r ascending with s = slot[t][r] >= 0 of recv_topk_w[r][s][j]
+ * (fp32 from +0) gives back the router's weight of every slot (0 where the slot was
+ * empty, out of range or dropped). Slots at or beyond max_tokens are skipped and raise
+ * ORACLE_FLAG_CAPACITY. */
+int32_t oracle_combine_weights(const float* recv_topk_w, const int32_t* slot, int32_t T, int32_t k,
+                               int32_t R, int32_t max_tokens, float* out) {
+    int32_t flags = 0;
+    for (int32_t t = 0; t < T; ++t) {
+        for (int32_t j = 0; j < k; ++j) out[(size_t)t * k + j] = 0.0f;
+        for (int32_t r = 0; r < R; ++r) {
+            int32_t s = slot[(size_t)t * R + r];
+            if (s < 0) continue;
+            if (s >= max_tokens) {
+                flags |= ORACLE_FLAG_CAPACITY;
+                continue;
+            }
+            const float* w = recv_topk_w + ((size_t)r * max_tokens + s) * k;
+            for (int32_t j = 0; j < k; ++j) out[(size_t)t * k + j] = out[(size_t)t * k + j] + w[j];
+        }
+    }
+    return flags;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Expert-major layout, permuted dispatch, receive-side permute, combine       */
 /* ------------------------------------------------------------------------- */

@@ -66,6 +66,15 @@ int32_t oracle_dispatch_nodes(const uint16_t* x, const float* prob_staging,
 int32_t oracle_combine(const uint16_t* y, const int32_t* slot, int32_t T, int32_t H, int32_t R,
                        int32_t max_tokens, uint16_t* out);
 
+/* combine of FP8 rows (codes [R][max][H], scales [R][max][H/128]): each row dequantised
+ * to fp32(e4m3(q) * scale), then as oracle_combine */
+int32_t oracle_combine_fp8(const uint8_t* y, const float* y_scales, const int32_t* slot, int32_t T,
+                           int32_t H, int32_t R, int32_t max_tokens, uint16_t* out);
+
+/* combined top-k weights: out[t][j] = fp32 sum over ranks ascending of recv_topk_w[r][slot][j] */
+int32_t oracle_combine_weights(const float* recv_topk_w, const int32_t* slot, int32_t T, int32_t k,
+                               int32_t R, int32_t max_tokens, float* out);
+
 /* expert-major layout: offsets [E+1] (exclusive sums of the per-expert counts, in
  * expert order) and expert_slot [T][k] = the stable position of (t, j) among the
  * entries of its expert, or -1. A repeated id in one token's row keeps only its

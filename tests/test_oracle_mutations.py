@@ -15,6 +15,7 @@ import test_oracle_formats as F
 import test_oracle_pages as G
 import test_oracle_path as PTH
 import test_oracle_permuted as PERM
+import test_oracle_combine_variants as CV
 
 MUTATIONS = [
     ("bf16 ties away from even",
@@ -93,6 +94,22 @@ MUTATIONS = [
      "        for (int32_t j = 0; j < k; ++j) {\n            if (expert_slot[(size_t)t * k + j] < 0) continue;\n            int64_t e = topk_idx[(size_t)t * k + j];\n            int32_t r = (int32_t)(e / (E / R));\n            int32_t p = permuted_row(expert_offsets, expert_slot, t, j, k, e, E, R);\n            if (p >= max_rows) {\n                flags |= ORACLE_FLAG_CAPACITY;\n                continue;\n            }\n            const uint16_t* row",
      "        for (int32_t j = k - 1; j >= 0; --j) {\n            if (expert_slot[(size_t)t * k + j] < 0) continue;\n            int64_t e = topk_idx[(size_t)t * k + j];\n            int32_t r = (int32_t)(e / (E / R));\n            int32_t p = permuted_row(expert_offsets, expert_slot, t, j, k, e, E, R);\n            if (p >= max_rows) {\n                flags |= ORACLE_FLAG_CAPACITY;\n                continue;\n            }\n            const uint16_t* row",
      [PERM.test_combine_permuted_term_order_is_the_topk_order]),
+    ("fp8 combine reads the next block's scale",
+     "float v = oracle_e4m3_to_f32(y[yr * H + h]) * y_scales[yr * nb + h / 128];",
+     "float v = oracle_e4m3_to_f32(y[yr * H + h]) * y_scales[yr * nb + (h / 128 + 1) % nb];",
+     [CV.test_combine_fp8_exact_closed_form_with_power_of_two_scales]),
+    ("fp8 combine in descending rank order",
+     "for (int32_t r = 0; r < R; ++r) {\n            int32_t s = slot[(size_t)t * R + r];\n            if (s < 0) continue;\n            if (s >= max_tokens) {\n                flags |= ORACLE_FLAG_CAPACITY;\n                continue;\n            }\n            size_t yr = (size_t)r * max_tokens + s;\n            for (int32_t h = 0; h < H; ++h) {\n                float v",
+     "for (int32_t r = R - 1; r >= 0; --r) {\n            int32_t s = slot[(size_t)t * R + r];\n            if (s < 0) continue;\n            if (s >= max_tokens) {\n                flags |= ORACLE_FLAG_CAPACITY;\n                continue;\n            }\n            size_t yr = (size_t)r * max_tokens + s;\n            for (int32_t h = 0; h < H; ++h) {\n                float v",
+     [CV.test_combine_fp8_order_is_ascending_on_a_crafted_token]),
+    ("combined weights keep the last rank's row",
+     "out[(size_t)t * k + j] = out[(size_t)t * k + j] + w[j];",
+     "out[(size_t)t * k + j] = w[j];",
+     [CV.test_combined_weights_return_the_router_weights]),
+    ("combined weights lose the capacity flag",
+     "flags |= ORACLE_FLAG_CAPACITY;\n                continue;\n            }\n            const float* w",
+     "flags |= 0;\n                continue;\n            }\n            const float* w",
+     [CV.test_combined_weights_drop_capacity_and_sum_in_rank_order]),
     ("expert drops the last weight",
      "for (int32_t j = 0; j < k; ++j) w = w + recv_topk_w[row * k + j];",
      "for (int32_t j = 0; j + 1 < k; ++j) w = w + recv_topk_w[row * k + j];",
@@ -122,7 +139,8 @@ def test_pins_catch_planted_mistake(tmp_path, monkeypatch, name, old, new, pins)
     for sym in ("oracle_f32_to_bf16", "oracle_bf16_to_f32", "oracle_f32_to_e4m3", "oracle_e4m3_to_f32",
                 "oracle_quantize_row_e4m3", "oracle_layout", "oracle_dispatch", "oracle_restripe_prob",
                 "oracle_dispatch_nodes", "oracle_combine", "oracle_expert_scale", "oracle_expert_layout",
-                "oracle_dispatch_permuted", "oracle_permute_received", "oracle_combine_permuted"):
+                "oracle_dispatch_permuted", "oracle_permute_received", "oracle_combine_permuted",
+                "oracle_combine_fp8", "oracle_combine_weights"):
         f_real, f_mut = getattr(real, sym), getattr(mutant, sym)
         f_mut.restype, f_mut.argtypes = f_real.restype, f_real.argtypes
     monkeypatch.setattr(oracle, "_lib", mutant)

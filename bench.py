@@ -458,7 +458,8 @@ def time_events(fn, n, flush, stream):
 
 
 def extra_stages(ep, dev, args, flush, peak):
-    """Per-stage device times of the other workloads (FP8 dispatch, restripe + node dispatch,
+    """Per-stage device times of the other workloads (FP8 dispatch and combine, combined weights,
+    restripe + node dispatch,
     skewed routing). Each is timed with CUDA events, L2 flushed before every launch."""
     stream = torch.cuda.current_stream()
     n = max(3, min(args.steps, 10))
@@ -481,7 +482,15 @@ def extra_stages(ep, dev, args, flush, peak):
     row = w.H + 4 * (w.H // 128)
     b = step_bytes(w.T, w.H, w.k, w.E, w.R, w.num_nodes, pairs, row_bytes_out=row)["dispatch"]
     res["dsv3_fp8_dispatch"] = gbs(b, ms)
-    del d, x, lay
+    # combine of the FP8 rows (the identity expert: the dispatch output itself) and the
+    # combined top-k weights, dsv3 shape
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    ms = time_events(lambda: ep.combine_fp8(d.recv_x, d.recv_scales, lay, w.max_tokens, out=out), n, flush, stream)
+    res["dsv3_fp8_combine"] = gbs(pairs * row + 4 * w.T * w.R + 2 * w.T * w.H, ms)
+    cw = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    ms = time_events(lambda: ep.combine_weights(d.recv_topk_w, lay, w.max_tokens, out=cw), n, flush, stream)
+    res["dsv3_combine_weights"] = gbs(pairs * 4 * w.k + 4 * w.T * w.R + 4 * w.T * w.k, ms)
+    del d, x, lay, out, cw
 
     # restripe + node dispatch (T=8192, H=7168, 8 nodes, P=128)
     w = workloads.make("restripe")

@@ -8,6 +8,8 @@ combine, with R virtual EP ranks held as slabs of one GPU's HBM:
   ep_restripe_prob   prob [T][nodes][P] -> [nodes][max_tokens][P]
   ep_dispatch_nodes  node-level dense / sparse (run-length) dispatch
   ep_combine         fp32 ascending-rank gather-reduce back to token order
+  ep_combine_fp8     the same from FP8 rows (E4M3 codes + 1x128 scales)
+  ep_combine_weights the received top-k weight rows summed back to token order
   ep_get_expert_layout / ep_dispatch_permuted / ep_permute_received /
   ep_combine_permuted  the expert-major (dispatch + permute) path, fused or split
 
@@ -21,9 +23,10 @@ from ._lib import (  # noqa: F401
     FLAG_CAPACITY, FLAG_TIMEOUT, FLAG_WORKSPACE, NODES_DENSE, NODES_SPARSE, EpError, ep_combine, ep_dispatch,
     ep_dispatch_nodes, ep_get_layout, ep_get_layout_noalloc, ep_layout_workspace_size, ep_restripe_prob, lib,
     ep_combine_permuted, ep_dispatch_permuted, ep_expert_layout_workspace_size, ep_get_expert_layout,
-    ep_permute_received,
+    ep_permute_received, ep_combine_fp8, ep_combine_weights,
 )
 from .api import (  # noqa: F401
-    Dispatched, Layout, alloc_dispatch, alloc_layout, combine, dispatch, get_layout, read_flags,
+    Dispatched, Layout, alloc_dispatch, alloc_layout, combine, combine_fp8, combine_weights, dispatch, get_layout,
+    read_flags,
 )
 from .build import LIB_PATH, build as build_library  # noqa: F401

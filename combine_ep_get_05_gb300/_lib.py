@@ -38,6 +38,7 @@ ABI_VERSION = 1
 EXPORTS = (
     "ep_abi_version", "ep_status_str", "ep_last_cuda_error", "ep_layout_workspace_size",
     "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_restripe_prob", "ep_dispatch_nodes", "ep_combine",
+    "ep_combine_fp8", "ep_combine_weights",
     "ep_expert_layout_workspace_size", "ep_get_expert_layout", "ep_dispatch_permuted", "ep_permute_received",
     "ep_combine_permuted",
 )
@@ -82,6 +83,8 @@ def lib():
                     "ep_restripe_prob": (i32, [P, i32, i32, i32, i32, P, P]),
                     "ep_dispatch_nodes": (i32, [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P, P]),
                     "ep_combine": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
+                    "ep_combine_fp8": (i32, [P, P, P, i32, i32, i32, i32, P, P, P]),
+                    "ep_combine_weights": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
                     "ep_expert_layout_workspace_size": (sz, [i32, i32]),
                     "ep_get_expert_layout": (i32, [P, i32, i32, i32, P, P, P, sz, P, P]),
                     "ep_dispatch_permuted": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, P]),
@@ -237,6 +240,31 @@ def ep_combine(y, slot, max_tokens, out, status=None, stream=None):
     _check("status", status, torch.int32, (1,), optional=True)
     rc = lib().ep_combine(_ptr(y), _ptr(slot), T, H, R, max_tokens, _ptr(out), _ptr(status), _stream(stream))
     _done("ep_combine", rc)
+
+
+def ep_combine_fp8(y, y_scales, slot, max_tokens, out, status=None, stream=None):
+    R, M, H = y.shape
+    T = slot.shape[0]
+    _check("y", y, torch.uint8, (R, max_tokens, H))
+    _check("y_scales", y_scales, torch.float32, (R, max_tokens, H // 128))
+    _check("slot", slot, torch.int32, (T, R))
+    _check("out", out, torch.bfloat16, (T, H))
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_combine_fp8(_ptr(y), _ptr(y_scales), _ptr(slot), T, H, R, max_tokens, _ptr(out), _ptr(status),
+                              _stream(stream))
+    _done("ep_combine_fp8", rc)
+
+
+def ep_combine_weights(recv_topk_w, slot, max_tokens, combined_w, status=None, stream=None):
+    R, M, k = recv_topk_w.shape
+    T = slot.shape[0]
+    _check("recv_topk_w", recv_topk_w, torch.float32, (R, max_tokens, k))
+    _check("slot", slot, torch.int32, (T, R))
+    _check("combined_w", combined_w, torch.float32, (T, k))
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_combine_weights(_ptr(recv_topk_w), _ptr(slot), T, k, R, max_tokens, _ptr(combined_w),
+                                  _ptr(status), _stream(stream))
+    _done("ep_combine_weights", rc)
 
 
 # --------------------------------------------------------------------------- expert-major path

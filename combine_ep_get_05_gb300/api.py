@@ -103,3 +103,23 @@ def combine(y: torch.Tensor, layout: Layout, max_tokens: int, out: Optional[torc
 def read_flags(status: torch.Tensor) -> int:
     """Synchronise and return the asynchronous EP_FLAG_* bits of a status word."""
     return int(status.item())
+
+
+def combine_fp8(y, y_scales, layout: Layout, max_tokens: int, out=None, status=None) -> torch.Tensor:
+    """Combine of FP8 expert outputs (E4M3 codes [R][max_tokens][H] + scales) into bf16 [T][H]."""
+    R, _, H = y.shape
+    T = layout.slot.shape[0]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=y.device)
+    L.ep_combine_fp8(y, y_scales, layout.slot, max_tokens, out, status)
+    return out
+
+
+def combine_weights(recv_topk_w, layout: Layout, max_tokens: int, out=None, status=None) -> torch.Tensor:
+    """The combined top-k weights [T][k]: the received weight rows summed back to token order."""
+    T = layout.slot.shape[0]
+    if out is None:
+        out = torch.empty((T, recv_topk_w.shape[2]), dtype=torch.float32, device=recv_topk_w.device)
+    L.ep_combine_weights(recv_topk_w, layout.slot, max_tokens, out, status)
+    return out
+

@@ -25,6 +25,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxSrc = 256;  // = largest R: every rank may contribute
 constexpr int kBatch = 8;  // source rows loaded together
 constexpr int kMinBlocks = 4;  // CTAs per SM the register budget is sized for
+constexpr int kBatchFp8 = 4;  // FP8 source rows loaded together (16 codes = half the bytes of 8 bf16)
 
 __device__ __forceinline__ void add8(float* acc, const uint4& v) {
     acc[0] = __fadd_rn(acc[0], ep::bf16_lo(v.x));
@@ -93,6 +94,126 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     }
 }
 
+// Combine of FP8 rows (E4M3 codes [R][max_tokens][H], one fp32 scale per 128 channels
+// [R][max_tokens][H/128]): as combine_kernel, with items of (token, 32 lanes x 16
+// channels); a lane loads 16 codes (one 16-byte vector) and its block's scale per source
+// row, converts the codes to fp32 exactly (E4M3 -> fp16 -> fp32), and adds
+// __fmul_rn(code, scale) to its accumulators, source rows in ascending rank order. (The
+// arithmetic stays scalar: a packed .f32x2 multiply feeding a packed add is contracted
+// into a fused multiply-add by the code generator, one rounding instead of two.)
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+    combine_fp8_kernel(const uint8_t* __restrict__ y, const float* __restrict__ y_scales,
+                       const int32_t* __restrict__ slot, int T, int H, int R, int max_tokens,
+                       uint16_t* __restrict__ out, int32_t* status) {
+    ep::grid_dependency_wait();  // dependent launch: the slabs are complete after this
+    __shared__ long long s_src[kWarps][kMaxSrc];
+    const int lane = ep::lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int nvec = H / 16;  // 16-code vectors per row
+    const int nblk = H / 128;
+    const int ngroups = (nvec + 31) / 32;
+    const long long items = static_cast<long long>(T) * ngroups;
+    const long long i0 = static_cast<long long>(blockIdx.x) * items / gridDim.x;
+    const long long i1 = static_cast<long long>(blockIdx.x + 1) * items / gridDim.x;
+    const uint4* ys = reinterpret_cast<const uint4*>(y);
+    uint4* os = reinterpret_cast<uint4*>(out);
+
+    for (long long it = i0 + warp; it < i1; it += kWarps) {
+        const int t = static_cast<int>(it / ngroups);
+        const int v = static_cast<int>(it - static_cast<long long>(t) * ngroups) * 32 + lane;
+        int ns = 0;
+        bool over_any = false;
+        for (int r0 = 0; r0 < R; r0 += 32) {
+            const int r = r0 + lane;
+            const int s = r < R ? slot[static_cast<size_t>(t) * R + r] : -1;
+            const bool over = s >= max_tokens;
+            over_any |= over;
+            const bool ok = s >= 0 && !over;
+            const uint32_t m = __ballot_sync(ep::kFullMask, ok);
+            if (ok) s_src[warp][ns + __popc(m & ep::lanemask_lt())] = static_cast<long long>(r) * max_tokens + s;
+            ns += __popc(m);
+        }
+        if (over_any && v == lane) ep::raise_flag(status, EP_FLAG_CAPACITY);
+        __syncwarp();
+
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        const int blk = v / 8;  // the lane's 16 channels lie in block v / 8
+        for (int d0 = 0; d0 < ns; d0 += kBatchFp8) {
+            uint4 buf[kBatchFp8];
+            float sc[kBatchFp8];
+#pragma unroll
+            for (int i = 0; i < kBatchFp8; ++i) {
+                if (d0 + i < ns && v < nvec) {
+                    const long long row = s_src[warp][d0 + i];
+                    buf[i] = ep::ld_stream_v4(ys + row * nvec + v);
+                    sc[i] = __ldg(y_scales + row * nblk + blk);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kBatchFp8; ++i) {
+                if (d0 + i < ns) {
+                    const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t a = ep::e4m3x2_to_f16x2(w[q] & 0xffffu);
+                        const uint32_t b = ep::e4m3x2_to_f16x2(w[q] >> 16);
+                        acc[4 * q + 0] = __fadd_rn(acc[4 * q + 0], __fmul_rn(ep::f16_to_f32(a & 0xffffu), sc[i]));
+                        acc[4 * q + 1] = __fadd_rn(acc[4 * q + 1], __fmul_rn(ep::f16_to_f32(a >> 16), sc[i]));
+                        acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], __fmul_rn(ep::f16_to_f32(b & 0xffffu), sc[i]));
+                        acc[4 * q + 3] = __fadd_rn(acc[4 * q + 3], __fmul_rn(ep::f16_to_f32(b >> 16), sc[i]));
+                    }
+                }
+            }
+        }
+        if (v < nvec) {
+            uint4 o0, o1;
+            o0.x = ep::pack_bf16x2_rn(acc[0], acc[1]);
+            o0.y = ep::pack_bf16x2_rn(acc[2], acc[3]);
+            o0.z = ep::pack_bf16x2_rn(acc[4], acc[5]);
+            o0.w = ep::pack_bf16x2_rn(acc[6], acc[7]);
+            o1.x = ep::pack_bf16x2_rn(acc[8], acc[9]);
+            o1.y = ep::pack_bf16x2_rn(acc[10], acc[11]);
+            o1.z = ep::pack_bf16x2_rn(acc[12], acc[13]);
+            o1.w = ep::pack_bf16x2_rn(acc[14], acc[15]);
+            uint4* dst = os + (static_cast<size_t>(t) * nvec + v) * 2;
+            ep::st_v4(dst, o0);
+            ep::st_v4(dst + 1, o1);
+        }
+        __syncwarp();
+    }
+}
+
+// Combined top-k weights: thread (t, j) adds recv_topk_w[r][slot[t][r]][j] over the ranks
+// in ascending order (fp32 from +0); the token's slot row is shared by its k threads.
+__global__ void __launch_bounds__(kThreads)
+    combine_weights_kernel(const float* __restrict__ w, const int32_t* __restrict__ slot, int T, int k, int R,
+                           int max_tokens, float* __restrict__ out, int32_t* status) {
+    ep::grid_dependency_wait();
+    const long long n = static_cast<long long>(T) * k;
+    for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * kThreads) {
+        const int t = static_cast<int>(i / k);
+        const int j = static_cast<int>(i - static_cast<long long>(t) * k);
+        float acc = 0.0f;
+        bool over_any = false;
+        for (int r = 0; r < R; ++r) {
+            const int s = __ldg(slot + static_cast<size_t>(t) * R + r);
+            if (s < 0) continue;
+            if (s >= max_tokens) {
+                over_any = true;
+                continue;
+            }
+            acc = __fadd_rn(acc, __ldg(w + (static_cast<size_t>(r) * max_tokens + s) * k + j));
+        }
+        if (over_any && j == 0) ep::raise_flag(status, EP_FLAG_CAPACITY);
+        out[i] = acc;
+    }
+}
+
+int g_fp8_blocks_per_sm[64] = {};
+
 int g_blocks_per_sm[64] = {};
 
 }  // namespace
@@ -120,4 +241,50 @@ extern "C" ep_status_t ep_combine(const void* y, const int32_t* slot, int32_t T,
     return launch_dependent(combine_kernel, dim3(grid), dim3(kThreads), 0, as_stream(stream),
                             static_cast<const uint16_t*>(y), slot, T, H, R, max_tokens, static_cast<uint16_t*>(out),
                             status);
+}
+
+extern "C" ep_status_t ep_combine_fp8(const uint8_t* y, const float* y_scales, const int32_t* slot, int32_t T,
+                                      int32_t H, int32_t R, int32_t max_tokens, void* out, int32_t* status,
+                                      void* stream) {
+    using namespace ep;
+    if (T < 0 || H <= 0 || H % 128 != 0 || R < 1 || R > 256 || max_tokens < 0) return EP_ERR_INVALID;
+    if (static_cast<long long>(R) * max_tokens > 0x7fffffffLL) return EP_ERR_INVALID;
+    if (T == 0) return EP_OK;
+    if (slot == nullptr || out == nullptr || (max_tokens > 0 && (y == nullptr || y_scales == nullptr)))
+        return EP_ERR_INVALID;
+    if (!aligned16_or_null(y) || !aligned16_or_null(y_scales) || !aligned16(slot) || !aligned16(out))
+        return EP_ERR_INVALID;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int per_sm = dev >= 0 && dev < 64 ? g_fp8_blocks_per_sm[dev] : 0;
+    if (per_sm == 0) {
+        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_fp8_kernel, kThreads, 0);
+        if (err != cudaSuccess) return cuda_fail(err);
+        if (per_sm < 1) per_sm = 1;
+        if (dev >= 0 && dev < 64) g_fp8_blocks_per_sm[dev] = per_sm;
+    }
+    const long long items = static_cast<long long>(T) * ((H / 16 + 31) / 32);
+    const long long want = (items + kWarps - 1) / kWarps;
+    const long long cap = static_cast<long long>(sm_count()) * per_sm;
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    return launch_dependent(combine_fp8_kernel, dim3(grid), dim3(kThreads), 0, as_stream(stream), y, y_scales, slot,
+                            T, H, R, max_tokens, static_cast<uint16_t*>(out), status);
+}
+
+extern "C" ep_status_t ep_combine_weights(const float* recv_topk_w, const int32_t* slot, int32_t T, int32_t k,
+                                          int32_t R, int32_t max_tokens, float* combined_w, int32_t* status,
+                                          void* stream) {
+    using namespace ep;
+    if (T < 0 || k < 1 || k > 32 || R < 1 || R > 256 || max_tokens < 0) return EP_ERR_INVALID;
+    if (static_cast<long long>(R) * max_tokens > 0x7fffffffLL) return EP_ERR_INVALID;
+    if (T == 0) return EP_OK;
+    if (slot == nullptr || combined_w == nullptr || (max_tokens > 0 && recv_topk_w == nullptr))
+        return EP_ERR_INVALID;
+    if (!aligned16_or_null(recv_topk_w) || !aligned16(slot) || !aligned16(combined_w)) return EP_ERR_INVALID;
+    const long long n = static_cast<long long>(T) * k;
+    const long long want = (n + kThreads - 1) / kThreads;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    return launch_dependent(combine_weights_kernel, dim3(grid), dim3(kThreads), 0, as_stream(stream), recv_topk_w,
+                            slot, T, k, R, max_tokens, combined_w, status);
 }

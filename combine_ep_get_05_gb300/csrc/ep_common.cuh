@@ -191,4 +191,19 @@ __device__ __forceinline__ uint32_t pack_e4m3x2_rn_sat(float lo, float hi) {
     return r;
 }
 
+// two OCP E4M3 codes (byte 0 -> low half, byte 1 -> high half) -> two fp16, exactly
+// (every E4M3 value is an fp16 value); then fp16 -> fp32, exactly
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    const uint16_t c = static_cast<uint16_t>(two_codes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+    return r;
+}
+__device__ __forceinline__ float f16_to_f32(uint32_t h) {
+    float f;
+    const uint16_t b = static_cast<uint16_t>(h);
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(b));
+    return f;
+}
+
 }  // namespace ep

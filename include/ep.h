@@ -261,6 +261,36 @@ ep_status_t ep_dispatch_nodes(const void* x, const float* prob_staging,
 ep_status_t ep_combine(const void* y, const int32_t* slot, int32_t T, int32_t H, int32_t R,
                        int32_t max_tokens, void* out, int32_t* status, void* stream);
 
+/* ep_combine_fp8 -- ep_combine for expert outputs kept in the FP8 row format of the
+ * dispatch ([PR #347] 3.2.1: H E4M3 codes and one fp32 scale per 128 channels). The
+ * pages show only the BF16 combine; this call reads each received row as the dispatch
+ * wrote it, dequantises every channel to fp32(e4m3(q) * scale) (one fp32 rounding) and
+ * reduces exactly as ep_combine does:
+ *   out[t][h] = bf16_rn( sum over r ascending with s = slot[t][r] >= 0 of
+ *                        fp32(e4m3(y[r][s][h]) * y_scales[r][s][h / 128]) )
+ *   y        E4M3 codes [R][max_tokens][H], H % 128 == 0
+ *   y_scales fp32 [R][max_tokens][H/128]
+ *   slot     int32 [T][R] from ep_get_layout;  out bf16 [T][H]
+ * R * max_tokens < 2^31. A slot >= max_tokens is skipped and raises EP_FLAG_CAPACITY.
+ * NaN codes (0x7F, 0xFF) are outside the contract. */
+ep_status_t ep_combine_fp8(const uint8_t* y, const float* y_scales, const int32_t* slot, int32_t T,
+                           int32_t H, int32_t R, int32_t max_tokens, void* out, int32_t* status,
+                           void* stream);
+
+/* ep_combine_weights -- the combined top-k weights: the combine also returns the weight
+ * rows the dispatch sent out ([PR #347] 2.1: the combine brings back what the dispatch
+ * sent), reduced to token order:
+ *   combined_w[t][j] = sum over r ascending with s = slot[t][r] >= 0 of
+ *                      recv_topk_w[r][s][j]            (fp32 from +0)
+ * Each rank's copy carries w_j for the slots whose expert it holds and +0 for the rest,
+ * so after ep_dispatch this is the router's weight (0 for empty, out-of-range or
+ * dropped slots).
+ *   recv_topk_w fp32 [R][max_tokens][k] (1 <= k <= 32); slot int32 [T][R];
+ *   combined_w fp32 [T][k]. A slot >= max_tokens is skipped and raises EP_FLAG_CAPACITY. */
+ep_status_t ep_combine_weights(const float* recv_topk_w, const int32_t* slot, int32_t T, int32_t k,
+                               int32_t R, int32_t max_tokens, float* combined_w, int32_t* status,
+                               void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Expert-major path: dispatch + permute (fused or split) and its combine     */
 /* ------------------------------------------------------------------------- */

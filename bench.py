@@ -550,6 +550,39 @@ def extra_stages(ep, dev, args, flush, peak):
     res["permuted_entries"] = entries
     del px, ps, pw, d, x, lay, out
 
+    # decode-sized batch (T=128 of the same shape): expert layout + dispatch + permute as two
+    # launches (one graph) against the single low-latency launch, then the weighted combine
+    Td = 128
+    w = workloads.make("dsv3", T=Td)
+    x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(w.topk_idx).to(dev)
+    tw = torch.from_numpy(w.topk_w).to(dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    eslot = torch.empty((Td, k), dtype=torch.int32, device=dev)
+    ews = torch.zeros(ep.ep_expert_layout_workspace_size(Td, E), dtype=torch.uint8, device=dev)
+    ep.ep_get_expert_layout(topk, E, off, eslot, ews)
+    offs = off.cpu().numpy()
+    Mp = int(max(offs[(r + 1) * epr] - offs[r * epr] for r in range(R)))
+    entries = int(offs[E])
+    px = torch.empty((R, Mp, H), dtype=torch.bfloat16, device=dev)
+    ps = torch.empty((R, Mp), dtype=torch.int32, device=dev)
+    pw = torch.empty((R, Mp), dtype=torch.float32, device=dev)
+    out = torch.empty((Td, H), dtype=torch.bfloat16, device=dev)
+    b_dp = Td * 2 * H + Td * k * 8 + 4 * (E + 1) + Td * k * 4 + entries * (2 * H + 8)
+
+    def two_launches():
+        ep.ep_get_expert_layout(topk, E, off, eslot, ews)
+        ep.ep_dispatch_permuted(x, topk, tw, off, eslot, E, R, Mp, px, ps, pw)
+
+    ms = time_events(two_launches, n, flush, stream)
+    res["decode128_layout_plus_dispatch_permuted"] = gbs(b_dp, ms)
+    ms = time_events(lambda: ep.ep_dispatch_permuted_ll(x, topk, tw, E, R, Mp, off, eslot, px, ps, pw), n, flush,
+                     stream)
+    res["decode128_dispatch_permuted_ll"] = gbs(b_dp, ms)
+    ms = time_events(lambda: ep.ep_combine_permuted(px, topk, tw, off, eslot, E, out), n, flush, stream)
+    res["decode128_combine_permuted_weighted"] = gbs(entries * 2 * H + Td * k * 16 + Td * 2 * H, ms)
+    del px, ps, pw, x, out
+
     # skewed routing dispatch + combine (T=16384, H=4096, R=64, max_tokens = hottest rank)
     w = workloads.make("skewed")
     x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)

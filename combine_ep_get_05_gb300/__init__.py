@@ -12,6 +12,7 @@ combine, with R virtual EP ranks held as slabs of one GPU's HBM:
   ep_combine_weights the received top-k weight rows summed back to token order
   ep_get_expert_layout / ep_dispatch_permuted / ep_permute_received /
   ep_combine_permuted  the expert-major (dispatch + permute) path, fused or split
+  ep_dispatch_permuted_ll  the same for a decode-sized batch in one launch
 
 The C ABI is include/ep.h (libep_gb300.so, built in-tree by build.py); the
 functions here with the same names are its ctypes binding, and api.py
@@ -23,7 +24,7 @@ from ._lib import (  # noqa: F401
     FLAG_CAPACITY, FLAG_TIMEOUT, FLAG_WORKSPACE, NODES_DENSE, NODES_SPARSE, EpError, ep_combine, ep_dispatch,
     ep_dispatch_nodes, ep_get_layout, ep_get_layout_noalloc, ep_layout_workspace_size, ep_restripe_prob, lib,
     ep_combine_permuted, ep_dispatch_permuted, ep_expert_layout_workspace_size, ep_get_expert_layout,
-    ep_permute_received, ep_combine_fp8, ep_combine_weights,
+    ep_permute_received, ep_combine_fp8, ep_combine_weights, ep_dispatch_permuted_ll,
 )
 from .api import (  # noqa: F401
     Dispatched, Layout, alloc_dispatch, alloc_layout, combine, combine_fp8, combine_weights, dispatch, get_layout,

@@ -40,7 +40,7 @@ EXPORTS = (
     "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_restripe_prob", "ep_dispatch_nodes", "ep_combine",
     "ep_combine_fp8", "ep_combine_weights",
     "ep_expert_layout_workspace_size", "ep_get_expert_layout", "ep_dispatch_permuted", "ep_permute_received",
-    "ep_combine_permuted",
+    "ep_combine_permuted", "ep_dispatch_permuted_ll",
 )
 
 
@@ -84,6 +84,7 @@ def lib():
                     "ep_dispatch_nodes": (i32, [P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P, P]),
                     "ep_combine": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
                     "ep_combine_fp8": (i32, [P, P, P, i32, i32, i32, i32, P, P, P]),
+                    "ep_dispatch_permuted_ll": (i32, [P, P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P]),
                     "ep_combine_weights": (i32, [P, P, i32, i32, i32, i32, P, P, P]),
                     "ep_expert_layout_workspace_size": (sz, [i32, i32]),
                     "ep_get_expert_layout": (i32, [P, i32, i32, i32, P, P, P, sz, P, P]),
@@ -345,3 +346,24 @@ def ep_combine_permuted(y, topk_idx, topk_w, expert_offsets, expert_slot, num_ex
     rc = lib().ep_combine_permuted(_ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(expert_offsets), _ptr(expert_slot),
                                    T, H, k, E, R, max_rows, _ptr(out), _ptr(status), _stream(stream))
     _done("ep_combine_permuted", rc)
+
+
+def ep_dispatch_permuted_ll(x, topk_idx, topk_w, num_experts, num_ranks, max_rows, expert_offsets, expert_slot, perm_x,
+                            perm_src=None, perm_w=None, status=None, stream=None):
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    E, R = num_experts, num_ranks
+    _check("x", x, torch.bfloat16, (T, H))
+    _check("topk_idx", topk_idx, torch.int64, (T, k))
+    _check("topk_w", topk_w, torch.float32, (T, k), optional=True)
+    _check("expert_offsets", expert_offsets, torch.int32, (E + 1,))
+    _check("expert_slot", expert_slot, torch.int32, (T, k))
+    _check("perm_x", perm_x, torch.bfloat16, (R, max_rows, H))
+    _check("perm_src", perm_src, torch.int32, (R, max_rows), optional=True)
+    _check("perm_w", perm_w, torch.float32, (R, max_rows), optional=True)
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_dispatch_permuted_ll(_ptr(x), _ptr(topk_idx), _ptr(topk_w), T, H, k, E, R, max_rows,
+                                       _ptr(expert_offsets), _ptr(expert_slot), _ptr(perm_x), _ptr(perm_src),
+                                       _ptr(perm_w), _ptr(status), _stream(stream))
+    _done("ep_dispatch_permuted_ll", rc)
+

@@ -543,6 +543,215 @@ __global__ void __launch_bounds__(kThreads, 4) combine_permuted_kernel(CombinePe
     }
 }
 
+// ---------------------------------------------------------------------------
+// Low-latency (decode-sized) dispatch + permute: one launch
+// ---------------------------------------------------------------------------
+// For a small batch (T <= kLLMaxTokens) every CTA computes the whole expert layout in
+// shared memory -- the per-warp expert masks and in-warp ranks of expert_layout_kernel,
+// chunk after chunk of 256 tokens with a running count per expert, then the offsets by a
+// block scan -- so no CTA waits on another and no workspace is needed. CTA 0 writes the
+// offsets and slots; CTA b then moves tokens b, b + gridDim.x, ...: warp 0 resolves the
+// token's expert-major rows and writes the metadata, and the 8 warps copy an eighth of
+// the row each to every destination. Same results as ep_get_expert_layout followed by
+// ep_dispatch_permuted.
+constexpr int kLLMaxTokens = 1024;
+constexpr int kLLMaxEntries = 8192;  // T * k
+
+struct LLArgs {
+    const uint16_t* x;
+    const int64_t* topk_idx;
+    const float* topk_w;
+    int T, H, k, E, R, max_rows;
+    int32_t* offsets;  // [E+1] out
+    int32_t* eslot;    // [T][k] out
+    uint16_t* perm_x;
+    int32_t* perm_src;
+    float* perm_w;
+    int32_t* status;
+};
+
+inline size_t ll_smem_bytes(int T, int k, int E) {
+    return (static_cast<size_t>(2 * kWarps) * E + ((E + 1 + 3) & ~3) + static_cast<size_t>(T) * k) * sizeof(int32_t);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) dispatch_permuted_ll_kernel(LLArgs a) {
+    grid_dependency_wait();  // dependent launch: inputs are ready after this
+    extern __shared__ uint32_t smem[];
+    uint32_t* s_emask = smem;                                              // [kWarps][E]
+    int32_t* s_wpref = reinterpret_cast<int32_t*>(smem + kWarps * a.E);  // [kWarps][E]
+    int32_t* s_cnt = s_wpref + kWarps * a.E;                             // [E+1]: counts, then offsets
+    int32_t* s_slot = s_cnt + ((a.E + 1 + 3) & ~3);                      // [T][k]: expert, then slot
+    __shared__ int32_t s_part[kWarps];
+    __shared__ long long s_row[kMaxTopk];
+    __shared__ int s_nd;
+    const int tid = static_cast<int>(threadIdx.x);
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int k = a.k;
+    const int E = a.E;
+    const int nvec = a.H / 8;
+    const int per_warp = (nvec + kWarps - 1) / kWarps;  // 16-byte vectors of a row per warp
+    const int v_lo = warp * per_warp;
+    const int v_hi = v_lo + per_warp < nvec ? v_lo + per_warp : nvec;
+
+    // the first token's row (this warp's slice) is requested before the layout work, so
+    // that its memory latency overlaps it
+    uint4 first[kUnroll];
+    if (static_cast<int>(blockIdx.x) < a.T) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(blockIdx.x) * a.H);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int v = v_lo + u * 32 + lane;
+            if (v < v_hi) first[u] = ld_stream_v4(src + v);
+        }
+    }
+
+    // 1. the expert layout of the whole batch, in shared memory
+    for (int e = tid; e < E; e += kThreads) s_cnt[e] = 0;
+    bool bad = false;
+    for (int c0 = 0; c0 < a.T; c0 += kThreads) {
+        const int t = c0 + tid;
+        for (int e = lane; e < E; e += 32) s_emask[warp * E + e] = 0u;
+        __syncthreads();
+        if (t < a.T) {
+            const long long* row = reinterpret_cast<const long long*>(a.topk_idx) + static_cast<size_t>(t) * k;
+            for (int j0 = 0; j0 < k; j0 += kBatch) {
+                long long ev[kBatch];  // eight ids in flight
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) ev[i] = j0 + i < k ? __ldg(row + j0 + i) : -1ll;
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) {
+                    const int j = j0 + i;
+                    if (j >= k) break;
+                    const long long e = ev[i];
+                    int x = -1;
+                    if (e >= 0) {
+                        if (e >= E) {
+                            bad = true;
+                        } else {
+                            bool rep = false;  // a repeat of an earlier slot of the row counts once
+#pragma unroll
+                            for (int ii = 0; ii < i; ++ii) rep |= ev[ii] == e;
+                            for (int jj = 0; jj < j0; ++jj) rep |= s_slot[t * k + jj] == static_cast<int>(e);
+                            if (rep) bad = true;
+                            else x = static_cast<int>(e);
+                        }
+                    }
+                    s_slot[t * k + j] = x;
+                    if (x >= 0) atomicOr(&s_emask[warp * E + x], 1u << lane);
+                }
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < E; e += kThreads) {
+            int run = s_cnt[e];
+            for (int w = 0; w < kWarps; ++w) {
+                s_wpref[w * E + e] = run;
+                run += __popc(s_emask[w * E + e]);
+            }
+            s_cnt[e] = run;
+        }
+        __syncthreads();
+        if (t < a.T) {
+            const uint32_t below = (1u << lane) - 1u;
+            for (int j = 0; j < k; ++j) {
+                const int x = s_slot[t * k + j];
+                s_slot[t * k + j] = x >= 0 ? s_wpref[warp * E + x] + __popc(s_emask[warp * E + x] & below) : -1;
+            }
+        }
+        __syncthreads();
+    }
+    // exclusive scan of the counts into the offsets (per-thread runs, then warp and block)
+    {
+        const int per = (E + kThreads - 1) / kThreads;
+        const int e0 = tid * per;
+        int sum = 0;
+        for (int i = 0; i < per; ++i)
+            if (e0 + i < E) sum += s_cnt[e0 + i];
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(kFullMask, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) s_part[warp] = incl;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += s_part[w];
+        int run = base + incl - sum;
+        for (int i = 0; i < per; ++i) {
+            if (e0 + i < E) {
+                const int c = s_cnt[e0 + i];
+                s_cnt[e0 + i] = run;
+                run += c;
+            }
+        }
+        if (tid == kThreads - 1) s_cnt[E] = base + incl;
+        __syncthreads();
+    }
+    if (blockIdx.x == 0) {
+        for (int e = tid; e <= E; e += kThreads) a.offsets[e] = s_cnt[e];
+        for (int i = tid; i < a.T * k; i += kThreads) a.eslot[i] = s_slot[i];
+        if (bad) raise_flag(a.status, EP_FLAG_BAD_EXPERT);
+    }
+
+    // 2. the rows
+    const int epr = E / a.R;
+    for (int t = static_cast<int>(blockIdx.x); t < a.T; t += static_cast<int>(gridDim.x)) {
+        if (warp == 0) {
+            bool ok = false, over = false;
+            long long rowi = 0;
+            if (lane < k) {
+                const int sl = s_slot[t * k + lane];
+                if (sl >= 0) {
+                    const int e = static_cast<int>(a.topk_idx[static_cast<size_t>(t) * k + lane]);
+                    const int r = e / epr;
+                    const int p = s_cnt[e] - s_cnt[r * epr] + sl;
+                    if (p < a.max_rows) {
+                        ok = true;
+                        rowi = static_cast<long long>(r) * a.max_rows + p;
+                    } else {
+                        over = true;
+                    }
+                }
+            }
+            const uint32_t m = __ballot_sync(kFullMask, ok);
+            if (ok) {
+                const int pos = __popc(m & lanemask_lt());
+                s_row[pos] = rowi;
+                if (a.perm_src != nullptr) a.perm_src[rowi] = t;
+                if (a.perm_w != nullptr) a.perm_w[rowi] = a.topk_w[static_cast<size_t>(t) * k + lane];
+            }
+            if (__any_sync(kFullMask, over) && lane == 0) raise_flag(a.status, EP_FLAG_CAPACITY);
+            if (lane == 0) s_nd = __popc(m);
+        }
+        __syncthreads();
+        const int nd = s_nd;
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H);
+        uint4* base = reinterpret_cast<uint4*>(a.perm_x);
+        for (int v0 = v_lo; v0 < v_hi; v0 += 32 * kUnroll) {
+            uint4 buf[kUnroll];
+            const bool prefetched = t == static_cast<int>(blockIdx.x) && v0 == v_lo;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int v = v0 + u * 32 + lane;
+                if (v < v_hi) buf[u] = prefetched ? first[u] : ld_stream_v4(src + v);
+            }
+            for (int d = 0; d < nd; ++d) {
+                uint4* dst = base + static_cast<size_t>(s_row[d]) * nvec;
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int v = v0 + u * 32 + lane;
+                    if (v < v_hi) st_v4(dst + v, buf[u]);
+                }
+            }
+        }
+        __syncthreads();  // s_row / s_nd are rewritten for the next token
+    }
+}
+
+bool g_ll_attr_set[64] = {};
+
 bool g_attr_set[64] = {};
 int g_combine_per_sm[64] = {};
 
@@ -673,4 +882,36 @@ extern "C" ep_status_t ep_combine_permuted(const void* y, const int64_t* topk_id
     const long long cap = static_cast<long long>(sm_count()) * per_sm;
     combine_permuted_kernel<<<static_cast<int>(want < cap ? want : cap), kThreads, 0, as_stream(stream)>>>(a);
     return check_launch();
+}
+
+extern "C" ep_status_t ep_dispatch_permuted_ll(const void* x, const int64_t* topk_idx, const float* topk_w,
+                                               int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
+                                               int32_t max_rows, int32_t* expert_offsets, int32_t* expert_slot,
+                                               void* perm_x, int32_t* perm_src, float* perm_w, int32_t* status,
+                                               void* stream) {
+    if (!perm_common_ok(T, H, k, E, R, max_rows) || T > kLLMaxTokens || T * k > kLLMaxEntries ||
+        E > kMaxExpertsPerm || expert_offsets == nullptr)
+        return EP_ERR_INVALID;
+    if (T > 0 && (x == nullptr || topk_idx == nullptr || expert_slot == nullptr || perm_x == nullptr ||
+                  (perm_w != nullptr && topk_w == nullptr)))
+        return EP_ERR_INVALID;
+    if (!aligned16_or_null(x) || !aligned16_or_null(perm_x) || !aligned16_or_null(topk_idx) ||
+        !aligned16_or_null(topk_w) || !aligned16(expert_offsets) || !aligned16_or_null(expert_slot) ||
+        !aligned16_or_null(perm_src) || !aligned16_or_null(perm_w))
+        return EP_ERR_INVALID;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !g_ll_attr_set[dev]) {
+        cudaError_t err = cudaFuncSetAttribute(dispatch_permuted_ll_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(ll_smem_bytes(kLLMaxTokens, kLLMaxEntries / kLLMaxTokens,
+                                                                              kMaxExpertsPerm)));
+        if (err != cudaSuccess) return cuda_fail(err);
+        g_ll_attr_set[dev] = true;
+    }
+    LLArgs a{static_cast<const uint16_t*>(x), topk_idx, topk_w, T, H, k, E, R, max_rows, expert_offsets, expert_slot,
+             static_cast<uint16_t*>(perm_x), perm_src, perm_w, status};
+    const int sms = sm_count();
+    const int grid = T < 1 ? 1 : (T < sms ? T : sms);
+    return launch_dependent(dispatch_permuted_ll_kernel, dim3(grid), dim3(kThreads), ll_smem_bytes(T, k, E),
+                            as_stream(stream), a);
 }

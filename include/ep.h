@@ -353,6 +353,22 @@ ep_status_t ep_permute_received(const void* recv_x, const int32_t* recv_src_idx,
                                 void* perm_x, int32_t* perm_src, float* perm_w, int32_t* status,
                                 void* stream);
 
+/* ep_dispatch_permuted_ll -- the low-latency (decode-sized) form of the expert-major
+ * dispatch: one launch computes the expert layout and moves the rows, with the same
+ * results as ep_get_expert_layout followed by ep_dispatch_permuted (expert_offsets,
+ * expert_slot, perm_x, perm_src, perm_w and the status flags). The pages name a
+ * low-latency mode for small decode batches ([PR #347] "low-latency" kernels beside the
+ * normal ones) without defining it; this is its single-GPU reading: no workspace, no
+ * second launch, every CTA recomputing the small layout in shared memory.
+ *   T <= 1024, T * k <= 8192, E <= 1024, E % R == 0; other arguments as
+ *   ep_get_expert_layout / ep_dispatch_permuted. expert_offsets int32 [E+1] and
+ *   expert_slot int32 [T][k] are outputs. T = 0 writes zero offsets. */
+ep_status_t ep_dispatch_permuted_ll(const void* x, const int64_t* topk_idx, const float* topk_w,
+                                    int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
+                                    int32_t max_rows, int32_t* expert_offsets, int32_t* expert_slot,
+                                    void* perm_x, int32_t* perm_src, float* perm_w, int32_t* status,
+                                    void* stream);
+
 /* ep_combine_permuted -- combine from expert-major slabs back to token order:
  *   out[t][h] = bf16_rn(acc), acc = 0; for j = 0 .. k-1 with a counted (t, j):
  *       acc = acc + topk_w[t][j] * float(y[r][p][h])   (topk_w given: one fp32

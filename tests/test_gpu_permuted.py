@@ -158,3 +158,73 @@ def test_expert_layout_workspace_reuse_and_bounded_wait():
         assert np.array_equal(host_bits(off), ELT["expert_offsets"])
         assert np.array_equal(host_bits(slot[:T]), ELT["expert_slot"])
         assert int(status.item()) == 0
+
+
+def run_ll(w, topk_np=None, max_rows=None):
+    """The single-launch decode-sized dispatch + permute against the oracle's layout and
+    dispatch + permute, every output compared bit for bit, between guard regions."""
+    topk_np = w.topk_idx if topk_np is None else topk_np
+    E, R, T, H, k = w.E, w.R, w.T, w.H, topk_np.shape[1]
+    EL = oracle.expert_layout(topk_np, E)
+    rows = oracle.rows_per_rank(EL["expert_offsets"], E, R)
+    M = max_rows if max_rows is not None else max(1, int(rows.max()))
+    off, boff = guarded((E + 1,), torch.int32, SENT_I32)
+    slot, bslot = guarded((T, k), torch.int32, SENT_I32)
+    px, bpx = guarded((R, M, H), torch.bfloat16, SENT_BF16)
+    ps, bps = guarded((R, M), torch.int32, SENT_I32)
+    pw, bpw = guarded((R, M), torch.float32, SENT_F32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.ep_dispatch_permuted_ll(dev_bf16(w.x), torch.from_numpy(topk_np).cuda(), torch.from_numpy(w.topk_w).cuda(), E, R,
+                               M, off, slot, px, ps, pw, st)
+    ref = oracle.dispatch_permuted(w.x, topk_np, w.topk_w, EL, E, R, M, fill_x=SENT_BF16, fill_idx=SENT_I32,
+                                   fill_w=SENT_F32)
+    assert int(st.item()) == (EL["flags"] | ref["flags"])
+    assert np.array_equal(host_bits(off), EL["expert_offsets"])
+    assert np.array_equal(host_bits(slot), EL["expert_slot"])
+    assert np.array_equal(host_bits(px), ref["perm_x"])
+    assert np.array_equal(host_bits(ps), ref["perm_src"])
+    assert np.array_equal(host_bits(pw).view(np.uint32), ref["perm_w"].view(np.uint32))
+    for b, v, f in ((boff, off, SENT_I32), (bslot, slot, SENT_I32), (bpx, px, SENT_BF16), (bps, ps, SENT_I32),
+                    (bpw, pw, SENT_F32)):
+        check_guards(b, v.numel(), f)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("dsv3", {"T": 128}),              # a decode batch at the full hidden size
+    ("dsv3", {"T": 1, "H": 1024}),
+    ("dsv3", {"T": 256, "H": 1024}),
+    ("dsv3", {"T": 257, "H": 512}),    # a second chunk of one token
+    ("dsv3", {"T": 1024, "H": 256}),   # the largest batch
+    ("skewed", {"T": 1000, "H": 256}),
+    ("restripe", {"T": 600, "H": 128}),  # E = 1024, empty slots
+])
+def test_low_latency_dispatch_permuted_matches_oracle(name, over):
+    run_ll(workloads.make(name, **over))
+
+
+def test_low_latency_dispatch_permuted_edge_cases():
+    rng = np.random.Generator(np.random.PCG64(33))
+    w = workloads.make("tiny", T=300, H=64)
+    t = w.topk_idx.copy()
+    t[3, 1] = t[3, 0]   # repeat
+    t[10, 2] = w.E + 5  # out of range
+    t[20, :] = -1       # routed nowhere
+    run_ll(w, t)
+    # k = 32 at the entry limit (T * k = 8192), E = 1024
+    w2 = workloads.make("tiny", T=256, H=32, E=1024, k=32, R=4)
+    run_ll(w2, workloads.routing_uniform(rng, 256, 1024, 32))
+    # capacity drops
+    w3 = workloads.make("skewed", T=800, H=64)
+    EL = oracle.expert_layout(w3.topk_idx, w3.E)
+    run_ll(w3, max_rows=int(oracle.rows_per_rank(EL["expert_offsets"], w3.E, w3.R).max()) // 2)
+    # empty batch: zero offsets; over the limits: refused
+    off = torch.full((17,), -9, dtype=torch.int32, device="cuda")
+    z = torch.zeros((0, 4), dtype=torch.int64, device="cuda")
+    ep.ep_dispatch_permuted_ll(torch.zeros((0, 8), dtype=torch.bfloat16, device="cuda"), z, None, 16, 4, 1, off,
+                               torch.zeros((0, 4), dtype=torch.int32, device="cuda"),
+                               torch.zeros((4, 1, 8), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert np.all(host_bits(off) == 0)
+    lib = ep.lib()
+    assert lib.ep_dispatch_permuted_ll(None, None, None, 1025, 8, 1, 16, 4, 1, None, None, None, None, None, None,
+                                       None) == ep.EP_ERR_INVALID

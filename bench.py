@@ -401,45 +401,72 @@ def run_ours(args, world, rank):
 
 
 def run_e2e(ep, w, dev, lay, disp, out, cstatus, flush, args, world, total_bytes):
-    """The same step through the public API as a user calls it, with the inputs copied in
-    from pinned host memory and the combined result copied back, every step."""
+    """The same step through the public API as a user pipeline calls it, with every step's
+    inputs copied in from pinned host memory and its combined result copied back. Steps are
+    double-buffered on two copy streams: step i+1's inputs travel host -> device while step
+    i computes and its result travels device -> host (the link is full duplex). The timed
+    region holds K whole steps, copies included; the value is K steps' bytes over it."""
     T, H, E, R, rpn, M = w.T, w.H, w.E, w.R, w.ranks_per_node, w.max_tokens
-    stream = torch.cuda.current_stream()
+    main = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     x_h = torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16).pin_memory()
     topk_h = torch.from_numpy(w.topk_idx).pin_memory()
     tw_h = torch.from_numpy(w.topk_w).pin_memory()
-    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    topk_d = torch.empty_like(topk_h, device=dev)
-    tw_d = torch.empty_like(tw_h, device=dev)
+    nb = 2
+    out_h = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(nb)]
+    x_d = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(nb)]
+    topk_d = [torch.empty_like(topk_h, device=dev) for _ in range(nb)]
+    tw_d = [torch.empty_like(tw_h, device=dev) for _ in range(nb)]
+    out_d = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(nb)]
+    ev = {n: [torch.cuda.Event() for _ in range(nb)] for n in ("in", "used", "done", "out")}
 
-    def e2e_step():
-        x_d.copy_(x_h, non_blocking=True)
-        topk_d.copy_(topk_h, non_blocking=True)
-        tw_d.copy_(tw_h, non_blocking=True)
-        ep.get_layout(topk_d, E, R, rpn, out=lay)
-        ep.dispatch(x_d, topk_d, tw_d, lay, M, out=disp)
-        ep.combine(disp.recv_x, lay, M, out=out, status=cstatus)
-        out_h.copy_(out, non_blocking=True)
+    def step(i):
+        b = i % nb
+        with torch.cuda.stream(s_in):
+            if i >= nb:
+                s_in.wait_event(ev["used"][b])  # step i-2 no longer reads these inputs
+            topk_d[b].copy_(topk_h, non_blocking=True)
+            tw_d[b].copy_(tw_h, non_blocking=True)
+            x_d[b].copy_(x_h, non_blocking=True)
+            ev["in"][b].record(s_in)
+        main.wait_event(ev["in"][b])
+        ep.get_layout(topk_d[b], E, R, rpn, out=lay)
+        ep.dispatch(x_d[b], topk_d[b], tw_d[b], lay, M, out=disp)
+        ev["used"][b].record(main)
+        if i >= nb:
+            main.wait_event(ev["out"][b])  # step i-2's result has left out_d[b]
+        ep.combine(disp.recv_x, lay, M, out=out_d[b], status=cstatus)
+        ev["done"][b].record(main)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["done"][b])
+            out_h[b].copy_(out_d[b], non_blocking=True)
+            ev["out"][b].record(s_out)
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(2 * nb):
+        step(i)
     torch.cuda.synchronize()
-    e2e_ms = []
-    for _ in range(args.steps):
-        flush()
-        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        z.record(stream)
-        z.synchronize()
-        e2e_ms.append(a.elapsed_time(z))
-    assert torch.equal(out_h, out.cpu())
-    t = max_over_ranks(world, statistics.mean(e2e_ms))
+    K = max(args.steps, 2 * nb)
+    flush()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(main)
+    s_in.wait_event(a)  # the first copy starts after the start event
+    for i in range(K):
+        step(i)
+    main.wait_stream(s_out)
+    z.record(main)
+    z.synchronize()
+    last = (K - 1) % nb
+    assert torch.equal(out_h[last], out_d[last].cpu())
+    assert torch.equal(out_h[last], out.cpu())  # the same step as the device-timed one
+    t = max_over_ranks(world, a.elapsed_time(z) / K)
     return {"value": round(world * total_bytes / (t * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(t, 4),
             "h2d_bytes_per_step": x_h.numel() * 2 + topk_h.numel() * 8 + tw_h.numel() * 4,
-            "d2h_bytes_per_step": out_h.numel() * 2,
-            "path": "pinned host -> cudaMemcpyAsync -> ep_get_layout, ep_dispatch, ep_combine -> pinned host"}
+            "d2h_bytes_per_step": out_h[0].numel() * 2, "steps": K,
+            "path": "pinned host -> cudaMemcpyAsync (copy stream) -> ep_get_layout, ep_dispatch, ep_combine -> "
+                    "pinned host (second copy stream); double-buffered, step i+1's input copy overlapping step i's "
+                    "compute and output copy; L2 flushed once before the timed steps"}
 
 
 def time_events(fn, n, flush, stream):

@@ -280,6 +280,23 @@ def test_node_path_full_size():
 
 # ----------------------------------------------------------------------------- layout specifics
 
+@pytest.mark.parametrize("T,E,k,R,rpn", [
+    (1000, 14, 3, 7, 7),      # R = 7: row widths that are no multiple of 4 or 16 bytes
+    (777, 66, 5, 33, 3),      # R = 33, 11 nodes of 3: vectors wrap across token rows
+    (5000, 96, 8, 96, 32),    # several tiles on fewer parts each; ragged last tile
+    (39 * 256 + 5, 160, 6, 160, 5),  # 40 tiles (parts = 1 or 2), N = 32
+    (300, 256, 9, 256, 256),  # the largest R, one node
+])
+def test_layout_odd_widths_and_tile_splits_match_oracle(T, E, k, R, rpn):
+    w = workloads.make("tiny", T=T, H=8, E=E, k=k, R=R, ranks_per_node=rpn)
+    L = oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node)
+    topk, lay = gpu_layout(w)
+    _assert_layout(w, lay, L)
+    # the same workspace again (the epoch advances, the counters are back at rest)
+    ep.get_layout(topk, w.E, w.R, w.ranks_per_node, out=lay)
+    _assert_layout(w, lay, L)
+
+
 def test_layout_empty_batch_and_workspace_reuse():
     lay = ep.alloc_layout(5000, 256, 32, 4)
     for T in (0, 1, 300, 5000, 17, 4096):

@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "ep_common.cuh"
+#include "ep_lookback.cuh"
 
 namespace {
 
@@ -42,12 +43,8 @@ constexpr int kTileWarps = kTileTokens / 32;
 constexpr int kMaxRanks = 256;
 constexpr int kMaxExperts = 8192;
 constexpr int kMaxTopk = 32;
-constexpr uint32_t kStateAggregate = 1u;
-constexpr uint32_t kStatePrefix = 2u;
 constexpr int kLookbackBatch = 16;
 constexpr int kIdsPerPass = 8;  // expert ids a thread holds in registers at once
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
-constexpr uint32_t kWaitLimitIters = 1u << 24;               // hard cap on polls
 
 struct LayoutArgs {
     const int64_t* topk_idx;
@@ -70,14 +67,6 @@ __host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~size_
 
 inline int num_tiles_for(int T) { return T > 0 ? (T + kTileTokens - 1) / kTileTokens : 1; }
 
-__device__ __forceinline__ unsigned long long pack_word(uint32_t epoch, uint32_t state, uint32_t v) {
-    return (static_cast<unsigned long long>(epoch) << 32) | (static_cast<unsigned long long>(state) << 30) |
-           static_cast<unsigned long long>(v & 0x3fffffffu);
-}
-__device__ __forceinline__ uint32_t word_epoch(unsigned long long w) { return static_cast<uint32_t>(w >> 32); }
-__device__ __forceinline__ uint32_t word_state(unsigned long long w) { return static_cast<uint32_t>(w >> 30) & 3u; }
-__device__ __forceinline__ uint32_t word_value(unsigned long long w) { return static_cast<uint32_t>(w) & 0x3fffffffu; }
-
 // Transpose of a 32 x 32 bit matrix held one row per lane (bit j of lane i =
 // A[i][j]): returns column `lane`, i.e. bit i of the result = A[i][lane]. Five
 // levels swap the off-diagonal blocks of size 16, 8, 4, 2, 1 between lane pairs.
@@ -91,20 +80,6 @@ __device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
         x = (lane & s) ? ((x & ~m) | ((y >> s) & m)) : ((x & m) | ((y & m) << s));
     }
     return x;
-}
-
-// Polls a tile word until it carries this call's epoch and a published state; returns
-// it, or 0 (no valid word has epoch 0) once the wait has run for kWaitLimitNs or
-// kWaitLimitIters polls. Kept out of line: it runs only when a word is not ready yet.
-__device__ __noinline__ unsigned long long wait_word(const unsigned long long* p, uint32_t epoch) {
-    const unsigned long long start = globaltimer_ns();
-    for (uint32_t polls = 1; polls < kWaitLimitIters; ++polls) {
-        if (polls > 16) __nanosleep(256);
-        const unsigned long long w = ld_relaxed_u64(p);
-        if (word_epoch(w) == epoch && word_state(w) != 0u) return w;
-        if (globaltimer_ns() - start > kWaitLimitNs) break;
-    }
-    return 0ull;
 }
 
 __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
@@ -224,33 +199,8 @@ __global__ void __launch_bounds__(kTileTokens) layout_kernel(LayoutArgs a) {
     // of the tile reads the same words, part 0 alone publishes the inclusive prefix
     if (tid < a.R) {
         const int r = tid;
-        uint32_t excl = 0;
         bool timed_out = false;
-        int j = tile - 1;
-        while (j >= 0 && !timed_out) {
-            const int nb = j + 1 < kLookbackBatch ? j + 1 : kLookbackBatch;
-            unsigned long long wv[kLookbackBatch];
-#pragma unroll
-            for (int i = 0; i < kLookbackBatch; ++i)
-                if (i < nb) wv[i] = ld_relaxed_u64(a.words + static_cast<size_t>(j - i) * a.R + r);
-            bool found_prefix = false;
-#pragma unroll
-            for (int i = 0; i < kLookbackBatch; ++i) {
-                if (i >= nb || found_prefix || timed_out) continue;
-                unsigned long long w = wv[i];
-                if (word_epoch(w) != epoch || word_state(w) == 0u) {
-                    w = wait_word(a.words + static_cast<size_t>(j - i) * a.R + r, epoch);
-                    if (w == 0ull) {
-                        timed_out = true;
-                        continue;
-                    }
-                }
-                excl += word_value(w);
-                if (word_state(w) == kStatePrefix) found_prefix = true;
-            }
-            if (found_prefix) break;
-            j -= nb;
-        }
+        const uint32_t excl = lookback_exclusive<kLookbackBatch>(a.words, a.R, tile, r, epoch, timed_out);
         if (timed_out) raise_flag(a.status, EP_FLAG_TIMEOUT);
         if (part == 0 && tile > 0 && !stalled)
             st_relaxed_u64(a.words + static_cast<size_t>(tile) * a.R + r, pack_word(epoch, kStatePrefix, excl + agg));

@@ -15,6 +15,7 @@
 #include <cstdio>
 
 #include "ep_common.cuh"
+#include "ep_lookback.cuh"
 #include "ep_scatter.cuh"
 
 namespace {
@@ -27,22 +28,10 @@ constexpr int kMaxExpertsPerm = 1024;  // expert layout: experts held per tile i
 constexpr int kMaxTopk = 32;
 constexpr int kUnroll = 8;
 constexpr int kBatch = 8;
-constexpr uint32_t kStateAggregate = 1u;
-constexpr uint32_t kStatePrefix = 2u;
 constexpr int kLookbackBatch = 8;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
-constexpr uint32_t kWaitLimitIters = 1u << 24;
 
 __host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 inline int num_tiles_for(int T) { return T > 0 ? (T + kThreads - 1) / kThreads : 1; }
-
-__device__ __forceinline__ unsigned long long pack_word(uint32_t epoch, uint32_t state, uint32_t v) {
-    return (static_cast<unsigned long long>(epoch) << 32) | (static_cast<unsigned long long>(state) << 30) |
-           static_cast<unsigned long long>(v & 0x3fffffffu);
-}
-__device__ __forceinline__ uint32_t word_epoch(unsigned long long w) { return static_cast<uint32_t>(w >> 32); }
-__device__ __forceinline__ uint32_t word_state(unsigned long long w) { return static_cast<uint32_t>(w >> 30) & 3u; }
-__device__ __forceinline__ uint32_t word_value(unsigned long long w) { return static_cast<uint32_t>(w) & 0x3fffffffu; }
 
 // ---------------------------------------------------------------------------
 // Expert layout
@@ -138,40 +127,8 @@ __global__ void __launch_bounds__(kThreads, 2) expert_layout_kernel(ExpertLayout
         const uint32_t agg = static_cast<uint32_t>(run);
         unsigned long long* my_word = a.words + static_cast<size_t>(tile) * a.E + e;
         if (!stalled) st_relaxed_u64(my_word, pack_word(epoch, tile == 0 ? kStatePrefix : kStateAggregate, agg));
-        uint32_t excl = 0;
         bool timed_out = false;
-        int j = tile - 1;
-        while (j >= 0 && !timed_out) {
-            const int nb = j + 1 < kLookbackBatch ? j + 1 : kLookbackBatch;
-            unsigned long long wv[kLookbackBatch];
-#pragma unroll
-            for (int i = 0; i < kLookbackBatch; ++i)
-                if (i < nb) wv[i] = ld_relaxed_u64(a.words + static_cast<size_t>(j - i) * a.E + e);
-            bool found_prefix = false;
-#pragma unroll
-            for (int i = 0; i < kLookbackBatch; ++i) {
-                if (i >= nb || found_prefix || timed_out) continue;
-                const unsigned long long* p = a.words + static_cast<size_t>(j - i) * a.E + e;
-                unsigned long long w = wv[i];
-                if (word_epoch(w) != epoch || word_state(w) == 0u) {
-                    const unsigned long long start = globaltimer_ns();
-                    uint32_t polls = 0;
-                    while (word_epoch(w) != epoch || word_state(w) == 0u) {
-                        if (++polls >= kWaitLimitIters || globaltimer_ns() - start > kWaitLimitNs) {
-                            timed_out = true;
-                            break;
-                        }
-                        if (polls > 16) __nanosleep(256);
-                        w = ld_relaxed_u64(p);
-                    }
-                    if (timed_out) break;
-                }
-                excl += word_value(w);
-                if (word_state(w) == kStatePrefix) found_prefix = true;
-            }
-            if (found_prefix) break;
-            j -= nb;
-        }
+        const uint32_t excl = lookback_exclusive<kLookbackBatch>(a.words, a.E, tile, e, epoch, timed_out);
         if (timed_out) raise_flag(a.status, EP_FLAG_TIMEOUT);
         if (tile > 0 && !stalled) st_relaxed_u64(my_word, pack_word(epoch, kStatePrefix, excl + agg));
         s_tpref[e] = static_cast<int32_t>(excl);

@@ -320,6 +320,69 @@ constexpr size_t kOffExperts = 256;
 constexpr size_t kOffNodes = kOffExperts + kMaxExperts * sizeof(int32_t);
 constexpr size_t kOffWords = kOffNodes + kMaxRanks * sizeof(int32_t);
 
+namespace {
+
+// Argument checks common to both entry points (the workspace is checked by the caller).
+bool layout_args_ok(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E, int32_t R, int32_t ranks_per_node,
+                    const int32_t* tokens_per_expert, const int32_t* tokens_per_rank, const int32_t* tokens_per_node,
+                    const uint8_t* is_token_in_rank, const uint8_t* is_token_in_node, const int32_t* slot) {
+    using namespace ep;
+    if (T < 0 || T >= (1 << 30) || k < 1 || k > kMaxTopk || R < 1 || R > kMaxRanks || E < R ||
+        E > kMaxExperts || E % R != 0 || ranks_per_node < 0 || ranks_per_node > R ||
+        (ranks_per_node > 0 && R % ranks_per_node != 0))
+        return false;
+    const bool nodes = ranks_per_node > 0;
+    if (tokens_per_expert == nullptr || tokens_per_rank == nullptr) return false;
+    if (T > 0 && (topk_idx == nullptr || is_token_in_rank == nullptr || slot == nullptr)) return false;
+    if (nodes && (tokens_per_node == nullptr || (T > 0 && is_token_in_node == nullptr))) return false;
+    return aligned16_or_null(topk_idx) && aligned16(tokens_per_expert) && aligned16(tokens_per_rank) &&
+           aligned16_or_null(tokens_per_node) && aligned16_or_null(is_token_in_rank) &&
+           aligned16_or_null(is_token_in_node) && aligned16_or_null(slot);
+}
+
+// Packs the arguments, points them into the workspace and launches the layout kernel.
+ep_status_t launch_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t E, int32_t R, int32_t ranks_per_node,
+                          int32_t* tokens_per_expert, int32_t* tokens_per_rank, int32_t* tokens_per_node,
+                          uint8_t* is_token_in_rank, uint8_t* is_token_in_node, int32_t* slot, char* ws,
+                          int32_t* status, cudaStream_t stream) {
+    using namespace ep;
+    const bool nodes = ranks_per_node > 0;
+    LayoutArgs a{};
+    a.topk_idx = topk_idx;
+    a.T = T;
+    a.k = k;
+    a.E = E;
+    a.R = R;
+    a.rpn = nodes ? ranks_per_node : 1;
+    a.N = nodes ? R / ranks_per_node : 0;
+    a.epr = E / R;
+    a.num_tiles = num_tiles_for(T);
+    a.parts = parts_for(a.num_tiles);
+    a.tokens_per_expert = tokens_per_expert;
+    a.tokens_per_rank = tokens_per_rank;
+    a.tokens_per_node = nodes ? tokens_per_node : nullptr;
+    a.in_rank = is_token_in_rank;
+    a.in_node = nodes ? is_token_in_node : nullptr;
+    a.slot = slot;
+    a.hdr = reinterpret_cast<ep_layout_ws_header_t*>(ws);
+    a.acc_expert = reinterpret_cast<int32_t*>(ws + kOffExperts);
+    a.acc_node = reinterpret_cast<int32_t*>(ws + kOffNodes);
+    a.words = reinterpret_cast<unsigned long long*>(ws + kOffWords);
+    a.status = status;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !g_smem_attr_set[dev]) {
+        const cudaError_t err = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     kMaxExperts * static_cast<int>(sizeof(int32_t)));
+        if (err != cudaSuccess) return cuda_fail(err);
+        g_smem_attr_set[dev] = true;
+    }
+    layout_kernel<<<a.num_tiles * a.parts, kTileTokens, static_cast<size_t>(E) * sizeof(int32_t), stream>>>(a);
+    return check_launch();
+}
+
+}  // namespace
+
 extern "C" size_t ep_layout_workspace_size(int32_t T, int32_t E, int32_t R, int32_t ranks_per_node) {
     (void)ranks_per_node;
     if (T < 0 || E <= 0 || R <= 0) return 0;
@@ -332,57 +395,15 @@ extern "C" ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t
                                      uint8_t* is_token_in_rank, uint8_t* is_token_in_node, int32_t* slot,
                                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
     using namespace ep;
-    if (T < 0 || T >= (1 << 30) || k < 1 || k > kMaxTopk || R < 1 || R > kMaxRanks || E < R ||
-        E > kMaxExperts || E % R != 0 || ranks_per_node < 0 || ranks_per_node > R ||
-        (ranks_per_node > 0 && R % ranks_per_node != 0))
+    if (!layout_args_ok(topk_idx, T, k, E, R, ranks_per_node, tokens_per_expert, tokens_per_rank, tokens_per_node,
+                        is_token_in_rank, is_token_in_node, slot))
         return EP_ERR_INVALID;
-    const bool nodes = ranks_per_node > 0;
-    if (tokens_per_expert == nullptr || tokens_per_rank == nullptr || workspace == nullptr)
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        workspace_bytes < ep_layout_workspace_size(T, E, R, ranks_per_node))
         return EP_ERR_INVALID;
-    if (T > 0 && (topk_idx == nullptr || is_token_in_rank == nullptr || slot == nullptr)) return EP_ERR_INVALID;
-    if (nodes && (tokens_per_node == nullptr || (T > 0 && is_token_in_node == nullptr))) return EP_ERR_INVALID;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EP_ERR_INVALID;
-    if (workspace_bytes < ep_layout_workspace_size(T, E, R, ranks_per_node)) return EP_ERR_INVALID;
-    if (!aligned16_or_null(topk_idx) || !aligned16(tokens_per_expert) || !aligned16(tokens_per_rank) ||
-        !aligned16_or_null(tokens_per_node) || !aligned16_or_null(is_token_in_rank) ||
-        !aligned16_or_null(is_token_in_node) || !aligned16_or_null(slot))
-        return EP_ERR_INVALID;
-
-    LayoutArgs a{};
-    a.topk_idx = topk_idx;
-    a.T = T;
-    a.k = k;
-    a.E = E;
-    a.R = R;
-    a.rpn = nodes ? ranks_per_node : 1;
-    a.N = nodes ? R / ranks_per_node : 0;
-    a.epr = E / R;
-    a.num_tiles = num_tiles_for(T);
-    a.tokens_per_expert = tokens_per_expert;
-    a.tokens_per_rank = tokens_per_rank;
-    a.tokens_per_node = nodes ? tokens_per_node : nullptr;
-    a.in_rank = is_token_in_rank;
-    a.in_node = nodes ? is_token_in_node : nullptr;
-    a.slot = slot;
-    char* ws = static_cast<char*>(workspace);
-    a.hdr = reinterpret_cast<ep_layout_ws_header_t*>(ws);
-    a.acc_expert = reinterpret_cast<int32_t*>(ws + kOffExperts);
-    a.acc_node = reinterpret_cast<int32_t*>(ws + kOffNodes);
-    a.words = reinterpret_cast<unsigned long long*>(ws + kOffWords);
-    a.status = status;
-
-    const size_t smem = static_cast<size_t>(E) * sizeof(int32_t);
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !g_smem_attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kMaxExperts * static_cast<int>(sizeof(int32_t)));
-        if (err != cudaSuccess) return cuda_fail(err);
-        g_smem_attr_set[dev] = true;
-    }
-    a.parts = parts_for(a.num_tiles);
-    layout_kernel<<<a.num_tiles * a.parts, kTileTokens, smem, as_stream(stream)>>>(a);
-    return check_launch();
+    return launch_layout(topk_idx, T, k, E, R, ranks_per_node, tokens_per_expert, tokens_per_rank, tokens_per_node,
+                         is_token_in_rank, is_token_in_node, slot, static_cast<char*>(workspace), status,
+                         as_stream(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -434,17 +455,8 @@ extern "C" ep_status_t ep_get_layout_noalloc(const int64_t* topk_idx, int32_t T,
                                              uint8_t* is_token_in_rank, uint8_t* is_token_in_node, int32_t* slot,
                                              int32_t* status, void* stream) {
     using namespace ep;
-    if (T < 0 || T >= (1 << 30) || k < 1 || k > kMaxTopk || R < 1 || R > kMaxRanks || E < R ||
-        E > kMaxExperts || E % R != 0 || ranks_per_node < 0 || ranks_per_node > R ||
-        (ranks_per_node > 0 && R % ranks_per_node != 0))
-        return EP_ERR_INVALID;
-    const bool nodes = ranks_per_node > 0;
-    if (tokens_per_expert == nullptr || tokens_per_rank == nullptr) return EP_ERR_INVALID;
-    if (T > 0 && (topk_idx == nullptr || is_token_in_rank == nullptr || slot == nullptr)) return EP_ERR_INVALID;
-    if (nodes && (tokens_per_node == nullptr || (T > 0 && is_token_in_node == nullptr))) return EP_ERR_INVALID;
-    if (!aligned16_or_null(topk_idx) || !aligned16(tokens_per_expert) || !aligned16(tokens_per_rank) ||
-        !aligned16_or_null(tokens_per_node) || !aligned16_or_null(is_token_in_rank) ||
-        !aligned16_or_null(is_token_in_node) || !aligned16_or_null(slot))
+    if (!layout_args_ok(topk_idx, T, k, E, R, ranks_per_node, tokens_per_expert, tokens_per_rank, tokens_per_node,
+                        is_token_in_rank, is_token_in_node, slot))
         return EP_ERR_INVALID;
     const size_t need = ep_layout_workspace_size(T, E, R, ranks_per_node);
     if (need > kNoAllocScratchBytes) return EP_ERR_SCRATCH;
@@ -453,41 +465,9 @@ extern "C" ep_status_t ep_get_layout_noalloc(const int64_t* topk_idx, int32_t T,
     ep_status_t st = scratch_address(&scratch);
     if (st != EP_OK) return st;
     // the array keeps the previous call's contents: zero the part this call uses
-    cudaError_t err = cudaMemsetAsync(scratch, 0, need, as_stream(stream));
+    const cudaError_t err = cudaMemsetAsync(scratch, 0, need, as_stream(stream));
     if (err != cudaSuccess) return cuda_fail(err);
-
-    LayoutArgs a{};
-    a.topk_idx = topk_idx;
-    a.T = T;
-    a.k = k;
-    a.E = E;
-    a.R = R;
-    a.rpn = nodes ? ranks_per_node : 1;
-    a.N = nodes ? R / ranks_per_node : 0;
-    a.epr = E / R;
-    a.num_tiles = num_tiles_for(T);
-    a.tokens_per_expert = tokens_per_expert;
-    a.tokens_per_rank = tokens_per_rank;
-    a.tokens_per_node = nodes ? tokens_per_node : nullptr;
-    a.in_rank = is_token_in_rank;
-    a.in_node = nodes ? is_token_in_node : nullptr;
-    a.slot = slot;
-    char* ws = static_cast<char*>(scratch);
-    a.hdr = reinterpret_cast<ep_layout_ws_header_t*>(ws);
-    a.acc_expert = reinterpret_cast<int32_t*>(ws + kOffExperts);
-    a.acc_node = reinterpret_cast<int32_t*>(ws + kOffNodes);
-    a.words = reinterpret_cast<unsigned long long*>(ws + kOffWords);
-    a.status = status;
-
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !g_smem_attr_set[dev]) {
-        err = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kMaxExperts * static_cast<int>(sizeof(int32_t)));
-        if (err != cudaSuccess) return cuda_fail(err);
-        g_smem_attr_set[dev] = true;
-    }
-    a.parts = parts_for(a.num_tiles);
-    layout_kernel<<<a.num_tiles * a.parts, kTileTokens, static_cast<size_t>(E) * sizeof(int32_t), as_stream(stream)>>>(a);
-    return check_launch();
+    return launch_layout(topk_idx, T, k, E, R, ranks_per_node, tokens_per_expert, tokens_per_rank, tokens_per_node,
+                         is_token_in_rank, is_token_in_node, slot, static_cast<char*>(scratch), status,
+                         as_stream(stream));
 }

@@ -101,3 +101,20 @@ def test_invalid_arguments_rejected_before_any_launch(libep):
     assert L.ep_dispatch(null, 0, null, null, null, 0, 64, 4, 16, 4, 16, fake, null, null, null, null, null,
                          null) == 0
     assert L.ep_combine(null, null, 0, 64, 4, 16, null, null, null) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No CPU fallback: with the library absent, loading it and calling an entry point raise."""
+    import torch
+
+    import combine_ep_get_05_gb300._lib as L
+
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "absent" / "libep_gb300.so"))
+    monkeypatch.setattr(L, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        L.lib()
+    with pytest.raises((RuntimeError, ValueError)):
+        L.ep_layout_workspace_size(16, 8, 4, 0)
+    with pytest.raises((RuntimeError, ValueError)):
+        L.ep_combine(torch.zeros((2, 1, 8), dtype=torch.bfloat16), torch.zeros((1, 2), dtype=torch.int32), 1,
+                     torch.zeros((1, 8), dtype=torch.bfloat16))

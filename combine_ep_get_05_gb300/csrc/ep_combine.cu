@@ -185,30 +185,44 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     }
 }
 
-// Combined top-k weights: thread (t, j) adds recv_topk_w[r][slot[t][r]][j] over the ranks
-// in ascending order (fp32 from +0); the token's slot row is shared by its k threads.
+// Combined top-k weights: a warp per token. Lanes read the token's slot row (lanes across
+// ranks) and compact the receiving ranks in ascending order with a ballot; lane j then
+// loads weight j of up to kBatch of those rows at once and adds them in rank order
+// (fp32 from +0).
 __global__ void __launch_bounds__(kThreads)
     combine_weights_kernel(const float* __restrict__ w, const int32_t* __restrict__ slot, int T, int k, int R,
                            int max_tokens, float* __restrict__ out, int32_t* status) {
     ep::grid_dependency_wait();
-    const long long n = static_cast<long long>(T) * k;
-    for (long long i = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; i < n;
-         i += static_cast<long long>(gridDim.x) * kThreads) {
-        const int t = static_cast<int>(i / k);
-        const int j = static_cast<int>(i - static_cast<long long>(t) * k);
-        float acc = 0.0f;
+    __shared__ long long s_src[kWarps][kMaxSrc];
+    const int lane = ep::lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    for (int t = static_cast<int>(blockIdx.x) * kWarps + warp; t < T; t += static_cast<int>(gridDim.x) * kWarps) {
+        int ns = 0;
         bool over_any = false;
-        for (int r = 0; r < R; ++r) {
-            const int s = __ldg(slot + static_cast<size_t>(t) * R + r);
-            if (s < 0) continue;
-            if (s >= max_tokens) {
-                over_any = true;
-                continue;
-            }
-            acc = __fadd_rn(acc, __ldg(w + (static_cast<size_t>(r) * max_tokens + s) * k + j));
+        for (int r0 = 0; r0 < R; r0 += 32) {
+            const int r = r0 + lane;
+            const int s = r < R ? __ldg(slot + static_cast<size_t>(t) * R + r) : -1;
+            const bool over = s >= max_tokens;
+            over_any |= over;
+            const bool ok = s >= 0 && !over;
+            const uint32_t m = __ballot_sync(ep::kFullMask, ok);
+            if (ok) s_src[warp][ns + __popc(m & ep::lanemask_lt())] = (static_cast<long long>(r) * max_tokens + s) * k;
+            ns += __popc(m);
         }
-        if (over_any && j == 0) ep::raise_flag(status, EP_FLAG_CAPACITY);
-        out[i] = acc;
+        if (__any_sync(ep::kFullMask, over_any) && lane == 0) ep::raise_flag(status, EP_FLAG_CAPACITY);
+        __syncwarp();
+        float acc = 0.0f;
+        for (int d0 = 0; d0 < ns; d0 += kBatch) {
+            float v[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                if (d0 + i < ns && lane < k) v[i] = __ldg(w + s_src[warp][d0 + i] + lane);
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i)
+                if (d0 + i < ns) acc = __fadd_rn(acc, v[i]);
+        }
+        if (lane < k) out[static_cast<size_t>(t) * k + lane] = acc;
+        __syncwarp();
     }
 }
 
@@ -281,8 +295,7 @@ extern "C" ep_status_t ep_combine_weights(const float* recv_topk_w, const int32_
     if (slot == nullptr || combined_w == nullptr || (max_tokens > 0 && recv_topk_w == nullptr))
         return EP_ERR_INVALID;
     if (!aligned16_or_null(recv_topk_w) || !aligned16(slot) || !aligned16(combined_w)) return EP_ERR_INVALID;
-    const long long n = static_cast<long long>(T) * k;
-    const long long want = (n + kThreads - 1) / kThreads;
+    const long long want = (static_cast<long long>(T) + kWarps - 1) / kWarps;
     const long long cap = static_cast<long long>(sm_count()) * 8;
     const int grid = static_cast<int>(want < cap ? want : cap);
     return launch_dependent(combine_weights_kernel, dim3(grid), dim3(kThreads), 0, as_stream(stream), recv_topk_w,

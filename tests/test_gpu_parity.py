@@ -286,6 +286,7 @@ def test_node_path_full_size():
     (5000, 96, 8, 96, 32),    # several tiles on fewer parts each; ragged last tile
     (39 * 256 + 5, 160, 6, 160, 5),  # 40 tiles (parts = 1 or 2), N = 32
     (300, 256, 9, 256, 256),  # the largest R, one node
+    (20000, 256, 8, 32, 4),   # 79 tiles: one CTA per tile
 ])
 def test_layout_odd_widths_and_tile_splits_match_oracle(T, E, k, R, rpn):
     w = workloads.make("tiny", T=T, H=8, E=E, k=k, R=R, ranks_per_node=rpn)

@@ -226,9 +226,8 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-int g_fp8_blocks_per_sm[64] = {};
-
-int g_blocks_per_sm[64] = {};
+std::atomic<int> g_fp8_blocks_per_sm[ep::kMaxDevices];
+std::atomic<int> g_blocks_per_sm[ep::kMaxDevices];
 
 }  // namespace
 
@@ -239,15 +238,9 @@ extern "C" ep_status_t ep_combine(const void* y, const int32_t* slot, int32_t T,
     if (T == 0) return EP_OK;
     if (slot == nullptr || out == nullptr || (max_tokens > 0 && y == nullptr)) return EP_ERR_INVALID;
     if (!aligned16_or_null(y) || !aligned16(slot) || !aligned16(out)) return EP_ERR_INVALID;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int per_sm = dev >= 0 && dev < 64 ? g_blocks_per_sm[dev] : 0;
-    if (per_sm == 0) {
-        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel, kThreads, 0);
-        if (err != cudaSuccess) return cuda_fail(err);
-        if (per_sm < 1) per_sm = 1;
-        if (dev >= 0 && dev < 64) g_blocks_per_sm[dev] = per_sm;
-    }
+    int per_sm = 1;
+    const ep_status_t occ = blocks_per_sm(g_blocks_per_sm, combine_kernel, kThreads, 0, &per_sm);
+    if (occ != EP_OK) return occ;
     const long long items = static_cast<long long>(T) * ((H / 8 + 31) / 32);
     const long long want = (items + kWarps - 1) / kWarps;
     const long long cap = static_cast<long long>(sm_count()) * per_sm;
@@ -268,15 +261,9 @@ extern "C" ep_status_t ep_combine_fp8(const uint8_t* y, const float* y_scales, c
         return EP_ERR_INVALID;
     if (!aligned16_or_null(y) || !aligned16_or_null(y_scales) || !aligned16(slot) || !aligned16(out))
         return EP_ERR_INVALID;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int per_sm = dev >= 0 && dev < 64 ? g_fp8_blocks_per_sm[dev] : 0;
-    if (per_sm == 0) {
-        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_fp8_kernel, kThreads, 0);
-        if (err != cudaSuccess) return cuda_fail(err);
-        if (per_sm < 1) per_sm = 1;
-        if (dev >= 0 && dev < 64) g_fp8_blocks_per_sm[dev] = per_sm;
-    }
+    int per_sm = 1;
+    const ep_status_t occ = blocks_per_sm(g_fp8_blocks_per_sm, combine_fp8_kernel, kThreads, 0, &per_sm);
+    if (occ != EP_OK) return occ;
     const long long items = static_cast<long long>(T) * ((H / 16 + 31) / 32);
     const long long want = (items + kWarps - 1) / kWarps;
     const long long cap = static_cast<long long>(sm_count()) * per_sm;

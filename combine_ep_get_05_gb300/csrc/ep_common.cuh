@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <utility>
@@ -16,6 +17,8 @@ constexpr unsigned kFullMask = 0xffffffffu;
 
 // ---------------------------------------------------------------- host side
 
+constexpr int kMaxDevices = 64;  // device ordinals the per-device caches below cover
+
 // SM count of the current device (cached per device ordinal).
 int sm_count();
 
@@ -24,6 +27,44 @@ ep_status_t cuda_fail(cudaError_t err);
 
 // EP_OK after a launch, or EP_ERR_CUDA if the launch was rejected.
 ep_status_t check_launch();
+
+// Ordinal of the current device, or -1 if there is none or it is >= kMaxDevices.
+inline int current_device() {
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices ? dev : -1;
+}
+
+// Per-device launch caches. Each is an array of kMaxDevices atomics owned by the caller
+// (static storage, so zero = "not known yet"). Host threads may make their first calls
+// on a device at the same time: both compute the same value and store it; the atomics
+// keep those accesses free of data races.
+
+// Lets `kernel` use `bytes` of dynamic shared memory, once per device.
+template <typename Kernel>
+ep_status_t ensure_dynamic_smem(std::atomic<int>* done, Kernel* kernel, int bytes) {
+    const int dev = current_device();
+    if (dev >= 0 && done[dev].load(std::memory_order_acquire) != 0) return EP_OK;
+    const cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (err != cudaSuccess) return cuda_fail(err);
+    if (dev >= 0) done[dev].store(1, std::memory_order_release);
+    return EP_OK;
+}
+
+// Resident CTAs per SM of `kernel` at `threads` threads and `smem` bytes of dynamic shared
+// memory on the current device (at least 1), computed once per device.
+template <typename Kernel>
+ep_status_t blocks_per_sm(std::atomic<int>* cache, Kernel* kernel, int threads, size_t smem, int* out) {
+    const int dev = current_device();
+    int n = dev >= 0 ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (n == 0) {
+        const cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+        if (err != cudaSuccess) return cuda_fail(err);
+        if (n < 1) n = 1;
+        if (dev >= 0) cache[dev].store(n, std::memory_order_relaxed);
+    }
+    *out = n;
+    return EP_OK;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned16_or_null(const void* p) { return p == nullptr || aligned16(p); }

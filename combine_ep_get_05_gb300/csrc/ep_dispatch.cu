@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a, 
     }
 }
 
-int g_fp8_per_sm[64] = {};
+std::atomic<int> g_fp8_per_sm[ep::kMaxDevices];
 
 int grid_for(int T, int blocks_per_sm) {
     const int want = (T + kWarps - 1) / kWarps;
@@ -337,15 +337,9 @@ extern "C" ep_status_t ep_dispatch(const void* x, ep_dtype_t out_dtype, const in
     a.recv_topk_w = recv_topk_w;
     a.status = status;
     if (fp8) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        int per_sm = dev >= 0 && dev < 64 ? g_fp8_per_sm[dev] : 0;
-        if (per_sm == 0) {
-            cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_fp8_kernel, kThreads, 0);
-            if (err != cudaSuccess) return cuda_fail(err);
-            if (per_sm < 1) per_sm = 1;
-            if (dev >= 0 && dev < 64) g_fp8_per_sm[dev] = per_sm;
-        }
+        int per_sm = 1;
+        const ep_status_t occ = blocks_per_sm(g_fp8_per_sm, dispatch_fp8_kernel, kThreads, 0, &per_sm);
+        if (occ != EP_OK) return occ;
         const long long resident = static_cast<long long>(sm_count()) * per_sm;
         const bool one_wave = static_cast<long long>(T) <= resident * kWarps;
         const int grid = one_wave ? static_cast<int>(resident) : grid_for(T, 8);

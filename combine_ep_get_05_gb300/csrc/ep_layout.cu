@@ -307,7 +307,7 @@ int parts_for(int num_tiles) {
     return parts;
 }
 
-bool g_smem_attr_set[64] = {};
+std::atomic<int> g_smem_attr_set[kMaxDevices];
 
 }  // namespace
 
@@ -369,14 +369,9 @@ ep_status_t launch_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t
     a.acc_node = reinterpret_cast<int32_t*>(ws + kOffNodes);
     a.words = reinterpret_cast<unsigned long long*>(ws + kOffWords);
     a.status = status;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !g_smem_attr_set[dev]) {
-        const cudaError_t err = cudaFuncSetAttribute(layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     kMaxExperts * static_cast<int>(sizeof(int32_t)));
-        if (err != cudaSuccess) return cuda_fail(err);
-        g_smem_attr_set[dev] = true;
-    }
+    const ep_status_t attr =
+        ensure_dynamic_smem(g_smem_attr_set, layout_kernel, kMaxExperts * static_cast<int>(sizeof(int32_t)));
+    if (attr != EP_OK) return attr;
     layout_kernel<<<a.num_tiles * a.parts, kTileTokens, static_cast<size_t>(E) * sizeof(int32_t), stream>>>(a);
     return check_launch();
 }
@@ -426,22 +421,32 @@ constexpr size_t kNoAllocScratchBytes = EP_LAYOUT_NOALLOC_SCRATCH_BYTES;
 static_assert(kNoAllocScratchBytes > kOffWords, "scratch must hold the fixed workspace part");
 
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {};
+void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_layout_scratch on the current device, looked up once per
-// device (host code must not use the symbol itself: on the host it names a
-// host-side shadow, not device memory).
-ep_status_t scratch_address(void** out) {
+// Device address of g_layout_scratch on the current device (host code must not use the
+// symbol itself: on the host it names a host-side shadow, not device memory). Outside
+// stream capture the address is looked up on every call (cudaGetSymbolAddress is a cheap
+// host call) and remembered, so a context created anew (after cudaDeviceReset) is picked
+// up at once. While `stream` is being captured the remembered address is used instead,
+// because the lookup may have to load the module, which a capture must not see; if no
+// call outside capture has been made on this device yet, the call is refused
+// (EP_ERR_INVALID) before anything is recorded into the graph.
+ep_status_t scratch_address(cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return cuda_fail(err);
-    if (dev < 0 || dev >= 64) return EP_ERR_INVALID;
+    if (dev < 0 || dev >= kMaxDevices) return EP_ERR_INVALID;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    err = cudaStreamIsCapturing(stream, &cap);
+    if (err != cudaSuccess) return cuda_fail(err);
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void* p = nullptr;
         err = cudaGetSymbolAddress(&p, g_layout_scratch);
         if (err != cudaSuccess || p == nullptr) return cuda_fail(err != cudaSuccess ? err : cudaErrorInvalidSymbol);
         g_scratch_ptr[dev] = p;
+    } else if (g_scratch_ptr[dev] == nullptr) {
+        return EP_ERR_INVALID;
     }
     *out = g_scratch_ptr[dev];
     return EP_OK;
@@ -462,7 +467,7 @@ extern "C" ep_status_t ep_get_layout_noalloc(const int64_t* topk_idx, int32_t T,
     if (need > kNoAllocScratchBytes) return EP_ERR_SCRATCH;
 
     void* scratch = nullptr;
-    ep_status_t st = scratch_address(&scratch);
+    ep_status_t st = scratch_address(as_stream(stream), &scratch);
     if (st != EP_OK) return st;
     // the array keeps the previous call's contents: zero the part this call uses
     const cudaError_t err = cudaMemsetAsync(scratch, 0, need, as_stream(stream));

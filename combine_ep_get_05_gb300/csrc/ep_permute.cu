@@ -707,10 +707,9 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_permuted_ll_kernel(LLArg
     }
 }
 
-bool g_ll_attr_set[64] = {};
-
-bool g_attr_set[64] = {};
-int g_combine_per_sm[64] = {};
+std::atomic<int> g_ll_attr_set[kMaxDevices];
+std::atomic<int> g_attr_set[kMaxDevices];
+std::atomic<int> g_combine_per_sm[kMaxDevices];
 
 int token_grid(long long work) {
     const long long want = (work + kWarps - 1) / kWarps;
@@ -747,15 +746,10 @@ extern "C" ep_status_t ep_get_expert_layout(const int64_t* topk_idx, int32_t T, 
     a.words = reinterpret_cast<unsigned long long*>(static_cast<char*>(workspace) + 256);
     a.status = status;
     const size_t smem = (static_cast<size_t>(E) * (2 * kWarps + 2) + static_cast<size_t>(k) * kThreads) * sizeof(int32_t);
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !g_attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(expert_layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (kMaxExpertsPerm * (2 * kWarps + 2) + kMaxTopk * kThreads) *
-                                                   static_cast<int>(sizeof(int32_t)));
-        if (err != cudaSuccess) return cuda_fail(err);
-        g_attr_set[dev] = true;
-    }
+    const ep_status_t attr = ensure_dynamic_smem(
+        g_attr_set, expert_layout_kernel,
+        (kMaxExpertsPerm * (2 * kWarps + 2) + kMaxTopk * kThreads) * static_cast<int>(sizeof(int32_t)));
+    if (attr != EP_OK) return attr;
     expert_layout_kernel<<<a.num_tiles, kThreads, smem, as_stream(stream)>>>(a);
     return check_launch();
 }
@@ -825,15 +819,9 @@ extern "C" ep_status_t ep_combine_permuted(const void* y, const int64_t* topk_id
         return EP_ERR_INVALID;
     CombinePermArgs a{static_cast<const uint16_t*>(y), topk_idx, topk_w, expert_offsets, expert_slot, T, H, k, E, R,
                       max_rows, static_cast<uint16_t*>(out), status};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    int per_sm = dev >= 0 && dev < 64 ? g_combine_per_sm[dev] : 0;
-    if (per_sm == 0) {
-        cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_permuted_kernel, kThreads, 0);
-        if (err != cudaSuccess) return cuda_fail(err);
-        if (per_sm < 1) per_sm = 1;
-        if (dev >= 0 && dev < 64) g_combine_per_sm[dev] = per_sm;
-    }
+    int per_sm = 1;
+    const ep_status_t occ = blocks_per_sm(g_combine_per_sm, combine_permuted_kernel, kThreads, 0, &per_sm);
+    if (occ != EP_OK) return occ;
     const long long items = static_cast<long long>(T) * ((H / 8 + 31) / 32);
     const long long want = (items + kWarps - 1) / kWarps;
     const long long cap = static_cast<long long>(sm_count()) * per_sm;
@@ -856,15 +844,10 @@ extern "C" ep_status_t ep_dispatch_permuted_ll(const void* x, const int64_t* top
         !aligned16_or_null(topk_w) || !aligned16(expert_offsets) || !aligned16_or_null(expert_slot) ||
         !aligned16_or_null(perm_src) || !aligned16_or_null(perm_w))
         return EP_ERR_INVALID;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !g_ll_attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(dispatch_permuted_ll_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(ll_smem_bytes(kLLMaxTokens, kLLMaxEntries / kLLMaxTokens,
-                                                                              kMaxExpertsPerm)));
-        if (err != cudaSuccess) return cuda_fail(err);
-        g_ll_attr_set[dev] = true;
-    }
+    const ep_status_t attr = ensure_dynamic_smem(
+        g_ll_attr_set, dispatch_permuted_ll_kernel,
+        static_cast<int>(ll_smem_bytes(kLLMaxTokens, kLLMaxEntries / kLLMaxTokens, kMaxExpertsPerm)));
+    if (attr != EP_OK) return attr;
     LLArgs a{static_cast<const uint16_t*>(x), topk_idx, topk_w, T, H, k, E, R, max_rows, expert_offsets, expert_slot,
              static_cast<uint16_t*>(perm_x), perm_src, perm_w, status};
     const int sms = sm_count();

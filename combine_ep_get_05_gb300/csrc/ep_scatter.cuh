@@ -106,16 +106,10 @@ template <class Spec>
 ep_status_t launch_scatter_rows(const Spec& spec, int items, cudaStream_t stream) {
     const size_t smem = static_cast<size_t>(kScatterStages) * spec.row_bytes;
     if (smem > kScatterMaxSmem || spec.row_bytes % 16 != 0) return EP_ERR_INVALID;
-    static bool attr_set[64] = {};  // one flag per device for each Spec instantiation
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t err = cudaFuncSetAttribute(scatter_rows_tma_kernel<Spec>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(kScatterMaxSmem));
-        if (err != cudaSuccess) return cuda_fail(err);
-        attr_set[dev] = true;
-    }
+    static std::atomic<int> attr_set[kMaxDevices];  // per device, for each Spec instantiation
+    const ep_status_t attr = ensure_dynamic_smem(attr_set, scatter_rows_tma_kernel<Spec>,
+                                                 static_cast<int>(kScatterMaxSmem));
+    if (attr != EP_OK) return attr;
     // one CTA per 1.5 rows: a third of the CTAs take a second row, whose load overlaps the
     // first row's stores, and the block scheduler still balances rows with different
     // numbers of destinations (measured best for 4096 x 7168 and 16384 x 4096 bf16 batches)

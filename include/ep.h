@@ -138,14 +138,18 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t
  * fixed-size array inside the library (EP_LAYOUT_NOALLOC_SCRATCH_BYTES of
  * device memory that every GPU which loads the library keeps until the process
  * exits). It never calls cudaMalloc, cudaFree or any allocating routine.
- *   - The first call on a device looks up that array's device address once
- *     (cudaGetSymbolAddress) with the device current; make that first call
- *     before any stream capture.
+ *   - Outside stream capture, every call looks up that array's device address
+ *     (cudaGetSymbolAddress, with the device current) and remembers it per
+ *     device. While `stream` is being captured into a CUDA graph the remembered
+ *     address is used: a captured call made before any uncaptured call on that
+ *     device returns EP_ERR_INVALID and records nothing, so make one call
+ *     outside capture first (and again after cudaDeviceReset, which gives the
+ *     array a new address).
  *   - Each call zero-fills the part of the array it uses (an async memset on
  *     `stream`), then launches the layout kernel.
  *   - Sizes whose workspace (ep_layout_workspace_size) exceeds
  *     EP_LAYOUT_NOALLOC_SCRATCH_BYTES are rejected with EP_ERR_SCRATCH before
- *     anything is launched (e.g. T up to ~126k tokens at R = 256, ~1M at R = 32).
+ *     anything is launched (T up to 126,720 tokens at R = 256, 1,014,528 at R = 32).
  *   - All calls on a device share the array: calls whose work can overlap on the
  *     GPU (different streams without ordering) race. Keep them on one stream.
  */

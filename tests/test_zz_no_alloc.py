@@ -3,25 +3,36 @@
 Some callers of this library cannot allocate device memory where they need the
 routing layout (a fixed, pre-planned memory budget without an allocator of its
 own, or a host runtime that can only pass pointers to arrays it already owns).
-ep_get_layout_noalloc serves them from a fixed array inside the library. This
-test calls it through the C ABI on two calls in a row -- with different sizes,
-so the second call starts from whatever the first left in the shared array --
-and checks every output bit for bit against ep_get_layout with its own
-workspace. It also checks that sizes beyond the fixed array are refused before
-anything is launched.
+ep_get_layout_noalloc serves them from a fixed array inside the library. The
+array keeps whatever the previous call left in it; every call zero-fills the
+part it uses before its kernel runs.
+
+These tests call it through the C ABI several times in a row, with different
+sizes (a large batch, then smaller ones whose regions of the array overlap the
+first), and check every output bit for bit against ep_get_layout with its own
+workspace, and for one case directly against the oracle; one case has no node
+split (ranks_per_node = 0). They also check that sizes beyond the fixed array
+are refused before anything is launched, and how the call behaves inside a
+CUDA graph capture.
 
 Collected last on purpose (file name), so a run that stops at the first
 failure has already run every other test. It passes alone in a fresh process
 and after the rest of the suite.
 """
 import ctypes
+import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
 import torch
 
 import combine_ep_get_05_gb300 as ep
+import oracle
 import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 pytestmark = pytest.mark.gpu
 
@@ -59,14 +70,15 @@ def _call_workspace(L, topk, E, R, rpn, b, stream):
     return rc, ws
 
 
-def test_noalloc_layout_matches_the_workspace_layout_on_two_calls_in_a_row():
+def test_noalloc_layout_matches_the_workspace_layout_on_calls_in_a_row():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     ep.build_library()
     L = ep.lib()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    cases = [workloads.make("dsv3", T=4096, H=8), workloads.make("skewed", T=3001, H=8)]
-    for w in cases:  # two calls in a row, different T, E, R and node counts
+    no_nodes = workloads.make("tiny", T=1500, H=8, E=64, k=6, R=16, ranks_per_node=0)
+    cases = [workloads.make("dsv3", T=4096, H=8), workloads.make("skewed", T=3001, H=8), no_nodes]
+    for w in cases:  # calls in a row, different T, E, R and node counts
         topk = torch.from_numpy(w.topk_idx).cuda()
         got = _buffers(w.T, w.E, w.R, w.ranks_per_node)
         ref = _buffers(w.T, w.E, w.R, w.ranks_per_node)
@@ -80,6 +92,11 @@ def test_noalloc_layout_matches_the_workspace_layout_on_two_calls_in_a_row():
             assert torch.equal(got[key], ref[key]), (w.name, key)
         assert int(got["status"].item()) == 0
         assert int(got["tpr"].sum().item()) == int(got["in_rank"].sum().item())
+    # the last case (no node split) straight against the oracle as well
+    O = oracle.layout(no_nodes.topk_idx, no_nodes.E, no_nodes.R, 0)
+    for key, name in (("tpe", "tokens_per_expert"), ("tpr", "tokens_per_rank"), ("in_rank", "is_token_in_rank"),
+                      ("slot", "slot")):
+        assert np.array_equal(got[key].cpu().numpy(), O[name]), name
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
@@ -91,3 +108,60 @@ def test_noalloc_refuses_sizes_beyond_its_scratch():
     rc = L.ep_get_layout_noalloc(fake, T, 8, E, R, 0, fake, fake, None, fake, None, fake, None, None)
     assert rc == ep.EP_ERR_SCRATCH
     assert b"EP_ERR_SCRATCH" in L.ep_status_str(rc)
+
+
+_CAPTURE_SCRIPT = r"""
+import ctypes, sys
+sys.path.insert(0, sys.argv[1])
+import torch
+import combine_ep_get_05_gb300 as ep
+import workloads
+L = ep.lib()
+w = workloads.make("dsv3", T=1000, H=8)
+topk = torch.from_numpy(w.topk_idx).cuda()
+N = w.R // w.ranks_per_node
+i32 = dict(dtype=torch.int32, device="cuda")
+out = [torch.zeros(w.E, **i32), torch.zeros(w.R, **i32), torch.zeros(N, **i32),
+       torch.zeros((w.T, w.R), dtype=torch.uint8, device="cuda"), torch.zeros((w.T, N), dtype=torch.uint8, device="cuda"),
+       torch.zeros((w.T, w.R), **i32)]
+status = torch.zeros(1, **i32)
+p = lambda t: ctypes.c_void_p(t.data_ptr())
+def call(stream):
+    return L.ep_get_layout_noalloc(p(topk), w.T, w.k, w.E, w.R, w.ranks_per_node, *[p(t) for t in out], p(status),
+                                   ctypes.c_void_p(stream.cuda_stream))
+s = torch.cuda.Stream()
+torch.cuda.synchronize()
+# a captured call before any uncaptured one on this device is refused and records nothing
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):
+    first = call(s)
+print("captured-first", first)
+# after one uncaptured call, a captured call records the layout into the graph
+assert call(torch.cuda.current_stream()) == ep.EP_OK
+torch.cuda.synchronize()
+ref = [t.clone() for t in out]
+for t in out:
+    t.fill_(0)
+g2 = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g2, stream=s):
+    second = call(s)
+print("captured-after", second)
+g2.replay()
+torch.cuda.synchronize()
+print("replay-equal", all(torch.equal(a, b) for a, b in zip(out, ref)), int(status.item()))
+"""
+
+
+def test_noalloc_inside_graph_capture():
+    """In a fresh process: a call captured before any uncaptured call is refused with
+    EP_ERR_INVALID (nothing recorded); once one uncaptured call has been made, a captured
+    call records the layout and the graph's replay reproduces the uncaptured result."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ep.build_library()
+    proc = subprocess.run([sys.executable, "-c", _CAPTURE_SCRIPT, ROOT], capture_output=True, text=True, timeout=300)
+    assert proc.returncode == 0, proc.stderr[-3000:]
+    lines = dict(line.split(" ", 1) for line in proc.stdout.strip().splitlines())
+    assert int(lines["captured-first"]) == ep.EP_ERR_INVALID
+    assert int(lines["captured-after"]) == ep.EP_OK
+    assert lines["replay-equal"] == "True 0"

@@ -79,6 +79,7 @@ def _load():
                 "oracle_dispatch_permuted": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]),
                 "oracle_permute_received": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P]),
                 "oracle_combine_permuted": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]),
+                "oracle_combine_send": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(lib, name)
@@ -320,4 +321,23 @@ def combine_permuted(y_bits, topk_idx, topk_w, EL: dict, E: int, R: int) -> tupl
     flags = int(_load().oracle_combine_permuted(
         _ptr(y), _ptr(ti), _ptr(tw), _ptr(_c(EL["expert_offsets"], np.int32)), _ptr(_c(EL["expert_slot"], np.int32)),
         T, H, k, E, R, max_rows, _ptr(out)))
+    return out, flags
+
+
+def combine_send(y_perm, D: dict, tokens_per_rank, EL: dict, T: int, E: int, R: int, weighted: bool = True,
+                 fill: int = 0) -> tuple:
+    """Send phase of a split combine: per rank and received row, the local experts' expert-major
+    rows reduced (weighted by the received top-k weights, or not) into one bf16 rank-level row.
+    Returns (y_rank [R][max_tokens][H] with unwritten rows at `fill`, flags)."""
+    yp = _c(y_perm, np.uint16)
+    _, max_rows, H = yp.shape
+    src = _c(D["recv_src_idx"], np.int32)
+    R_, M = src.shape
+    k = D["recv_topk_idx"].shape[2]
+    tw = _c(D["recv_topk_w"], np.float32) if weighted else None
+    out = np.full((R, M, H), fill, np.uint16)
+    flags = int(_load().oracle_combine_send(
+        _ptr(yp), _ptr(src), _ptr(_c(D["recv_topk_idx"], np.int32)), _ptr(tw), _ptr(_c(tokens_per_rank, np.int32)),
+        _ptr(_c(EL["expert_offsets"], np.int32)), _ptr(_c(EL["expert_slot"], np.int32)), T, H, k, E, R, M, max_rows,
+        _ptr(out)))
     return out, flags

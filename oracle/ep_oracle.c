@@ -604,6 +604,63 @@ int32_t oracle_combine_permuted(const uint16_t* y, const int64_t* topk_idx, cons
     return flags;
 }
 
+/* The send phase of a split (hook-mode) combine ([PR #347] 2.1: in hook mode the send
+ * phase runs first and returns, the receive phase runs later as its own step). The
+ * combine's receive phase is oracle_combine: it reads one row per (token, rank) from
+ * the rank-level slabs. The send phase fills those rows: rank r takes, for every row
+ * s < min(tokens_per_rank[r], max_tokens) it received (t = recv_src_idx[r][s]), the
+ * expert-major rows of that token's local experts -- the rows the receive-side permute
+ * wrote, p = expert_offsets[e] - expert_offsets[r*(E/R)] + expert_slot[t][j] for every
+ * slot j with local id l = recv_topk_idx[r][s][j] >= 0, e = r*(E/R) + l -- and reduces
+ * them into its rank-level row:
+ *   acc = 0 (fp32); for j = 0, 1, ..., k-1 with such a row p:
+ *       term = float(y_perm[r][p][h]), times recv_topk_w[r][s][j] (one fp32 multiply)
+ *              when weights are given
+ *       acc  = acc + term
+ *   y_rank[r][s][h] = bf16_rn(acc)
+ * Reading: the pages split the combine into send and receive without fixing where a
+ * rank's local experts are reduced; the rank-level receive rows are bf16 like every other
+ * combine input, so each rank rounds its partial sum once. Rows p >= max_rows were never
+ * written: skipped with ORACLE_FLAG_CAPACITY. Rows s beyond the count are not written. */
+int32_t oracle_combine_send(const uint16_t* y_perm, const int32_t* recv_src_idx,
+                            const int32_t* recv_topk_idx, const float* recv_topk_w,
+                            const int32_t* tokens_per_rank, const int32_t* expert_offsets,
+                            const int32_t* expert_slot, int32_t T, int32_t H, int32_t k,
+                            int32_t E, int32_t R, int32_t max_tokens, int32_t max_rows,
+                            uint16_t* y_rank) {
+    int32_t flags = 0;
+    int32_t epr = E / R;
+    float* acc = (float*)malloc((size_t)H * sizeof(float) + 1);
+    (void)T;
+    for (int32_t r = 0; r < R; ++r) {
+        int32_t n = tokens_per_rank[r] < max_tokens ? tokens_per_rank[r] : max_tokens;
+        for (int32_t s = 0; s < n; ++s) {
+            size_t row = (size_t)r * max_tokens + s;
+            int32_t t = recv_src_idx[row];
+            for (int32_t h = 0; h < H; ++h) acc[h] = 0.0f;
+            for (int32_t j = 0; j < k; ++j) {
+                int32_t l = recv_topk_idx[row * k + j];
+                if (l < 0 || expert_slot[(size_t)t * k + j] < 0) continue;
+                int32_t e = r * epr + l;
+                int32_t p = expert_offsets[e] - expert_offsets[r * epr] + expert_slot[(size_t)t * k + j];
+                if (p >= max_rows) {
+                    flags |= ORACLE_FLAG_CAPACITY;
+                    continue;
+                }
+                const uint16_t* src = y_perm + ((size_t)r * max_rows + p) * H;
+                for (int32_t h = 0; h < H; ++h) {
+                    float term = oracle_bf16_to_f32(src[h]);
+                    if (recv_topk_w != NULL) term = term * recv_topk_w[row * k + j];
+                    acc[h] = acc[h] + term;
+                }
+            }
+            for (int32_t h = 0; h < H; ++h) y_rank[row * H + h] = oracle_f32_to_bf16(acc[h]);
+        }
+    }
+    free(acc);
+    return flags;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Harness expert (between dispatch and combine; not a step of the path)      */
 /* ------------------------------------------------------------------------- */

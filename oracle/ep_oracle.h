@@ -104,6 +104,16 @@ int32_t oracle_combine_permuted(const uint16_t* y, const int64_t* topk_idx, cons
                                 int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
                                 int32_t max_rows, uint16_t* out);
 
+/* send phase of a split combine: each rank reduces, per received row, its local experts'
+ * expert-major rows (slot order, weighted by recv_topk_w when not NULL) into one bf16 row
+ * of its rank-level slab y_rank [R][max_tokens][H]; oracle_combine is the receive phase */
+int32_t oracle_combine_send(const uint16_t* y_perm, const int32_t* recv_src_idx,
+                            const int32_t* recv_topk_idx, const float* recv_topk_w,
+                            const int32_t* tokens_per_rank, const int32_t* expert_offsets,
+                            const int32_t* expert_slot, int32_t T, int32_t H, int32_t k,
+                            int32_t E, int32_t R, int32_t max_tokens, int32_t max_rows,
+                            uint16_t* y_rank);
+
 /* the test harness's stand-in expert (not part of the path): every received row
  * scaled by the sum, in j order, of its top-k weights on that rank */
 void oracle_expert_scale(const void* recv_x, int32_t in_fp8, const float* recv_scales,

@@ -16,6 +16,7 @@ import test_oracle_pages as G
 import test_oracle_path as PTH
 import test_oracle_permuted as PERM
 import test_oracle_combine_variants as CV
+import test_oracle_split_combine as SPL
 
 MUTATIONS = [
     ("bf16 ties away from even",
@@ -110,6 +111,26 @@ MUTATIONS = [
      "flags |= ORACLE_FLAG_CAPACITY;\n                continue;\n            }\n            const float* w",
      "flags |= 0;\n                continue;\n            }\n            const float* w",
      [CV.test_combined_weights_drop_capacity_and_sum_in_rank_order]),
+    ("combine send drops the weight",
+     "if (recv_topk_w != NULL) term = term * recv_topk_w[row * k + j];",
+     "if (recv_topk_w != NULL) term = term * 1.0f;",
+     [SPL.test_combine_send_power_of_two_weights_closed_form]),
+    ("combine send sums slots in reverse",
+     "            for (int32_t j = 0; j < k; ++j) {\n                int32_t l = recv_topk_idx[row * k + j];\n                if (l < 0 || expert_slot[(size_t)t * k + j] < 0) continue;\n                int32_t e = r * epr + l;\n                int32_t p = expert_offsets[e] - expert_offsets[r * epr] + expert_slot[(size_t)t * k + j];\n                if (p >= max_rows) {\n                    flags |= ORACLE_FLAG_CAPACITY;\n                    continue;\n                }\n                const uint16_t* src",
+     "            for (int32_t j = k - 1; j >= 0; --j) {\n                int32_t l = recv_topk_idx[row * k + j];\n                if (l < 0 || expert_slot[(size_t)t * k + j] < 0) continue;\n                int32_t e = r * epr + l;\n                int32_t p = expert_offsets[e] - expert_offsets[r * epr] + expert_slot[(size_t)t * k + j];\n                if (p >= max_rows) {\n                    flags |= ORACLE_FLAG_CAPACITY;\n                    continue;\n                }\n                const uint16_t* src",
+     [SPL.test_combine_send_term_order_is_the_slot_order]),
+    ("combine send indexes rank 0's expert offsets",
+     "int32_t p = expert_offsets[e] - expert_offsets[r * epr] + expert_slot[(size_t)t * k + j];\n                if (p >= max_rows) {\n                    flags |= ORACLE_FLAG_CAPACITY;\n                    continue;\n                }\n                const uint16_t* src",
+     "int32_t p = expert_offsets[e] - expert_offsets[0] + expert_slot[(size_t)t * k + j];\n                if (p >= max_rows) {\n                    flags |= ORACLE_FLAG_CAPACITY;\n                    continue;\n                }\n                const uint16_t* src",
+     [SPL.test_combine_send_inverts_the_receive_side_permute, SPL.test_combine_send_identity_rows_closed_form]),
+    ("combine send accumulates in bf16",
+     "if (recv_topk_w != NULL) term = term * recv_topk_w[row * k + j];\n                    acc[h] = acc[h] + term;",
+     "if (recv_topk_w != NULL) term = term * recv_topk_w[row * k + j];\n                    acc[h] = oracle_bf16_to_f32(oracle_f32_to_bf16(acc[h] + term));",
+     [SPL.test_combine_send_power_of_two_weights_closed_form]),
+    ("combine send loses the capacity flag",
+     "flags |= ORACLE_FLAG_CAPACITY;\n                    continue;\n                }\n                const uint16_t* src",
+     "flags |= 0;\n                    continue;\n                }\n                const uint16_t* src",
+     [SPL.test_combine_send_capacity_drops_and_flags]),
     ("expert drops the last weight",
      "for (int32_t j = 0; j < k; ++j) w = w + recv_topk_w[row * k + j];",
      "for (int32_t j = 0; j + 1 < k; ++j) w = w + recv_topk_w[row * k + j];",
@@ -140,7 +161,7 @@ def test_pins_catch_planted_mistake(tmp_path, monkeypatch, name, old, new, pins)
                 "oracle_quantize_row_e4m3", "oracle_layout", "oracle_dispatch", "oracle_restripe_prob",
                 "oracle_dispatch_nodes", "oracle_combine", "oracle_expert_scale", "oracle_expert_layout",
                 "oracle_dispatch_permuted", "oracle_permute_received", "oracle_combine_permuted",
-                "oracle_combine_fp8", "oracle_combine_weights"):
+                "oracle_combine_fp8", "oracle_combine_weights", "oracle_combine_send"):
         f_real, f_mut = getattr(real, sym), getattr(mutant, sym)
         f_mut.restype, f_mut.argtypes = f_real.restype, f_real.argtypes
     monkeypatch.setattr(oracle, "_lib", mutant)

@@ -244,10 +244,144 @@ def cpu_baseline(w, budget_s=12.0, tokens=None):
     total = sum(b.values())
     return {
         "value": round(total / (spent / steps) / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "host": host_cpu(),
         "sample": f"{steps} oracle steps (layout+dispatch+identity combine) on {tokens} of the {w.T} tokens, "
                   f"single-threaded C, {spent:.1f} s",
         "tokens_per_s": round(tokens / (spent / steps), 1),
     }
+
+
+def host_cpu():
+    """The host's core count and CPU model, as /proc/cpuinfo (or the platform) gives them."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model Name", "cpu model"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key:
+                    model = line.split(":", 1)[1].strip()
+                    break
+            if model:
+                break
+        if model is None:  # Arm: implementer / part numbers
+            imp = [line.split(":")[1].strip() for line in info.splitlines() if line.startswith("CPU implementer")]
+            part = [line.split(":")[1].strip() for line in info.splitlines() if line.startswith("CPU part")]
+            if imp and part:
+                model = f"Arm implementer {imp[0]} part {part[0]}"
+    except OSError:
+        pass
+    import platform
+
+    return {"nproc": os.cpu_count(), "model": model or platform.processor() or platform.machine()}
+
+
+def oracle_stage_baselines():
+    """The oracle (single-threaded C, one host core) on a bounded sample of each extra stage's
+    workload, in the same unit (algorithmic GB/s by the same formulas, scaled to the sample)."""
+    import oracle
+
+    oracle.build()
+    res = {"host": host_cpu(), "cores_used": 1}
+
+    def timed(fn, min_s=0.25):
+        """Mean seconds per call over as many calls as fill min_s (at least one)."""
+        n, spent, out = 0, 0.0, None
+        while n == 0 or spent < min_s:
+            t0 = time.perf_counter()
+            out = fn()
+            spent += time.perf_counter() - t0
+            n += 1
+        return spent / n, out
+
+    def entry(bytes_, sec, sample):
+        return {"gbs": round(bytes_ / sec / 1e9, 3), "s": round(sec, 3), "sample": sample}
+
+    S = 512  # tokens per sample for the large-row stages
+    w = workloads.make("dsv3_fp8")
+    x, ti, tw = w.x[:S], w.topk_idx[:S], w.topk_w[:S]
+    L = oracle.layout(ti, w.E, w.R, w.ranks_per_node)
+    pairs = int(L["tokens_per_rank"].sum())
+    sec, D = timed(lambda: oracle.dispatch(x, ti, tw, L["slot"], w.E, w.R, S, fp8=True))
+    row = w.H + 4 * (w.H // 128)
+    res["dsv3_fp8_dispatch"] = entry(step_bytes(S, w.H, w.k, w.E, w.R, w.num_nodes, pairs, row)["dispatch"], sec,
+                                     f"first {S} of {w.T} tokens")
+    sec, _ = timed(lambda: oracle.combine_fp8(D["recv_x"], D["recv_scales"], L["slot"], S))
+    res["dsv3_fp8_combine"] = entry(pairs * row + 4 * S * w.R + 2 * S * w.H, sec, f"first {S} of {w.T} tokens")
+    sec, _ = timed(lambda: oracle.combine_weights(D["recv_topk_w"], L["slot"], S))
+    res["dsv3_combine_weights"] = entry(pairs * 4 * w.k + 4 * S * w.R + 4 * S * w.k, sec, f"first {S} of {w.T} tokens")
+    del D
+
+    w = workloads.make("restripe")
+    Nn, P = w.num_nodes, w.prob.shape[2]
+    sec, st = timed(lambda: oracle.restripe_prob(w.prob, w.T))
+    res["restripe_prob"] = entry(2 * w.T * Nn * P * 4, sec, f"all {w.T} tokens")
+    L = oracle.layout(w.topk_idx[:S], w.E, w.R, w.ranks_per_node)
+    stS = np.ascontiguousarray(st[:, :S])
+    routed = int(L["is_token_in_node"].sum())
+    for name, dense, dests in (("node_dispatch_sparse", False, routed), ("node_dispatch_dense", True, Nn * S)):
+        sec, _ = timed(lambda dense=dense: oracle.dispatch_nodes(w.x[:S], stS, L["is_token_in_node"], S,
+                                                                 w.chunk_tokens, dense=dense))
+        b = S * 2 * w.H + dests * (2 * w.H + 2 * P * 4) + (0 if dense else S * Nn)
+        res[name] = entry(b, sec, f"first {S} of {w.T} tokens (2 chunks)")
+    del st, stS
+
+    w = workloads.make("dsv3")
+    T, H, k, E, R = w.T, w.H, w.k, w.E, w.R
+    sec, EL = timed(lambda: oracle.expert_layout(w.topk_idx, E))
+    res["expert_layout"] = entry(T * k * 12 + 4 * (E + 1), sec, f"all {T} tokens")
+    ti, x, tw = w.topk_idx[:S], w.x[:S], w.topk_w[:S]
+    ELs = oracle.expert_layout(ti, E)
+    Mp = int(oracle.rows_per_rank(ELs["expert_offsets"], E, R).max())
+    entries = int(ELs["expert_offsets"][E])
+    sec, PX = timed(lambda: oracle.dispatch_permuted(x, ti, tw, ELs, E, R, Mp))
+    res["dispatch_permuted"] = entry(S * 2 * H + S * k * 16 + entries * (2 * H + 8), sec, f"first {S} of {T} tokens")
+    L = oracle.layout(ti, E, R, w.ranks_per_node)
+    pairs = int(L["tokens_per_rank"].sum())
+    D = oracle.dispatch(x, ti, tw, L["slot"], E, R, S)
+    sec, _ = timed(lambda: oracle.permute_received(D, L["tokens_per_rank"], ELs, S, E, R, Mp))
+    res["permute_received"] = entry(pairs * (2 * H + 4 + 8 * k) + S * k * 4 + entries * (2 * H + 8), sec,
+                                    f"first {S} of {T} tokens")
+    sec, _ = timed(lambda: oracle.combine_permuted(PX["perm_x"], ti, tw, ELs, E, R))
+    res["combine_permuted_weighted"] = entry(entries * 2 * H + S * k * 16 + S * 2 * H, sec, f"first {S} of {T} tokens")
+    sec, _ = timed(lambda: oracle.combine_send(PX["perm_x"], D, L["tokens_per_rank"], ELs, S, E, R))
+    res["combine_send_weighted"] = entry(entries * 2 * H + pairs * (2 * H + 4 + 8 * k) + S * k * 4 + 4 * (E + 1), sec,
+                                         f"first {S} of {T} tokens")
+    del PX, D
+
+    w = workloads.make("dsv3", T=128)
+    sec, ELd = timed(lambda: oracle.expert_layout(w.topk_idx, E))
+    Mp = int(oracle.rows_per_rank(ELd["expert_offsets"], E, R).max())
+    entries = int(ELd["expert_offsets"][E])
+    sec2, PX = timed(lambda: oracle.dispatch_permuted(w.x, w.topk_idx, w.topk_w, ELd, E, R, Mp))
+    res["decode128_dispatch_permuted"] = entry(128 * 2 * H + 128 * k * 8 + 4 * (E + 1) + 128 * k * 4 +
+                                               entries * (2 * H + 8), sec + sec2, "all 128 tokens")
+    sec, _ = timed(lambda: oracle.combine_permuted(PX["perm_x"], w.topk_idx, w.topk_w, ELd, E, R))
+    res["decode128_combine_weighted"] = entry(entries * 2 * H + 128 * k * 16 + 128 * 2 * H, sec, "all 128 tokens")
+    del PX
+
+    w = workloads.make("skewed")
+    ti, x, tw = w.topk_idx[:S], w.x[:S], w.topk_w[:S]
+    sec, L = timed(lambda: oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node))
+    b = step_bytes(w.T, w.H, w.k, w.E, w.R, w.num_nodes, int(L["tokens_per_rank"].sum()))
+    res["skewed_layout"] = entry(b["layout"], sec, f"all {w.T} tokens")
+    L = oracle.layout(ti, w.E, w.R, w.ranks_per_node)
+    pairs = int(L["tokens_per_rank"].sum())
+    b = step_bytes(S, w.H, w.k, w.E, w.R, w.num_nodes, pairs)
+    sec, D = timed(lambda: oracle.dispatch(x, ti, tw, L["slot"], w.E, w.R, S))
+    res["skewed_dispatch"] = entry(b["dispatch"], sec, f"first {S} of {w.T} tokens")
+    sec, _ = timed(lambda: oracle.combine(D["recv_x"], L["slot"], S))
+    res["skewed_combine"] = entry(b["combine"], sec, f"first {S} of {w.T} tokens")
+    del D
+
+    w = workloads.make("tiny")
+    sec, L = timed(lambda: oracle.layout(w.topk_idx, w.E, w.R, w.ranks_per_node))
+    sec2, D = timed(lambda: oracle.dispatch(w.x, w.topk_idx, w.topk_w, L["slot"], w.E, w.R, w.T))
+    sec3, _ = timed(lambda: oracle.combine(D["recv_x"], L["slot"], w.T))
+    pairs = int(L["tokens_per_rank"].sum())
+    res["tiny_step"] = entry(sum(step_bytes(w.T, w.H, w.k, w.E, w.R, w.num_nodes, pairs).values()), sec + sec2 + sec3,
+                             f"all {w.T} tokens")
+    return res
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -368,6 +502,7 @@ def run_ours(args, world, rank):
                   "frac_of_hbm_peak": round(b[s] / (mean[s] * 1e-3) / 1e9 / peak, 4)} for s in stage_ms}
 
     e2e = None if args.no_e2e else run_e2e(ep, w, dev, lay, disp, out, cstatus, flush, args, world, total_bytes)
+    sustained = None if args.skip_extra else sustained_step(ep, dev, args, flush, peak)
     extra = {} if args.skip_extra else extra_stages(ep, dev, args, flush, peak)
 
     line = {
@@ -389,6 +524,7 @@ def run_ours(args, world, rank):
                      if peak_kind == "measured" else "fallback", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "alg_bytes_per_launch": b[dom], "traffic_note": traffic_note},
+        "sustained": sustained,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
@@ -397,6 +533,8 @@ def run_ours(args, world, rank):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
+        if not args.skip_extra:
+            line["cpu_baseline"]["per_stage"] = oracle_stage_baselines()
     return line
 
 
@@ -469,6 +607,40 @@ def run_e2e(ep, w, dev, lay, disp, out, cstatus, flush, args, world, total_bytes
                     "compute and output copy; L2 flushed once before the timed steps"}
 
 
+def sustained_step(ep, dev, args, flush, peak, K=8):
+    """K whole steps (layout -> dispatch -> combine) back to back in one graph, each on its
+    own input and output buffers (K x 505 MB touched, far beyond L2), L2 flushed only before
+    the replay: every step's writes are written back to HBM inside the timed region (by the
+    steps that follow; the last step's output is the only data possibly left in L2)."""
+    stream = torch.cuda.current_stream()
+    w = workloads.make("dsv3")
+    T, H, E, k, R, rpn, M = w.T, w.H, w.E, w.k, w.R, w.ranks_per_node, w.max_tokens
+    x0 = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    topk0 = torch.from_numpy(w.topk_idx).to(dev)
+    tw0 = torch.from_numpy(w.topk_w).to(dev)
+    sets = []
+    for _ in range(K):
+        sets.append({"x": x0.clone(), "topk": topk0.clone(), "tw": tw0.clone(),
+                     "lay": ep.alloc_layout(T, E, R, rpn, dev), "d": ep.alloc_dispatch(R, M, H, k, device=dev),
+                     "out": torch.empty((T, H), dtype=torch.bfloat16, device=dev)})
+
+    def run():
+        for st in sets:
+            ep.get_layout(st["topk"], E, R, rpn, out=st["lay"])
+            ep.dispatch(st["x"], st["topk"], st["tw"], st["lay"], M, out=st["d"])
+            ep.combine(st["d"].recv_x, st["lay"], M, out=st["out"])
+
+    ms = time_events(run, max(3, min(args.steps, 10)), flush, stream) / K
+    pairs = int(sets[0]["lay"].tokens_per_rank.sum().item())
+    assert torch.equal(sets[-1]["out"], sets[0]["out"])
+    total = sum(step_bytes(T, H, k, E, R, w.num_nodes, pairs).values())
+    del sets
+    return {"steps_per_replay": K, "ms_per_step": round(ms, 4), "alg_bytes_per_step": total,
+            "gbs": round(total / (ms * 1e-3) / 1e9, 1), "frac_of_hbm_peak": round(total / (ms * 1e-3) / 1e9 / peak, 4),
+            "tokens_per_s": round(T / (ms * 1e-3), 1),
+            "timing": f"{K} steps on {K} distinct buffer sets in one graph; L2 flushed before each replay only"}
+
+
 def time_events(fn, n, flush, stream):
     """Mean device time of fn, captured in a CUDA graph, L2 flushed before each replay."""
     g = capture(fn)
@@ -527,8 +699,19 @@ def extra_stages(ep, dev, args, flush, peak):
     prob = torch.from_numpy(w.prob).to(dev)
     Nn, T, M, P, H = w.num_nodes, w.T, w.max_tokens, w.prob.shape[2], w.H
     staging = torch.empty((Nn, M, P), dtype=torch.float32, device=dev)
-    ms = time_events(lambda: ep.ep_restripe_prob(prob, M, staging), n, flush, stream)
-    res["restripe_prob"] = gbs(2 * T * Nn * P * 4, ms)
+    ms1 = time_events(lambda: ep.ep_restripe_prob(prob, M, staging), n, flush, stream)
+    # the kernel's own rate: 8 restripes back to back on 8 distinct buffer pairs (536 MB, well
+    # beyond L2) in one graph, so each launch also pays the write-back of the previous one's
+    # output; a single launch after a flush is dominated by the ~6 us event/launch floor
+    NB = 8
+    probs = [prob] + [prob.clone() for _ in range(NB - 1)]
+    stagings = [staging] + [torch.empty_like(staging) for _ in range(NB - 1)]
+    ms8 = time_events(lambda: [ep.ep_restripe_prob(probs[i], M, stagings[i]) for i in range(NB)], n, flush, stream)
+    res["restripe_prob"] = gbs(2 * T * Nn * P * 4, ms8 / NB)
+    res["restripe_prob"].update({"timing": f"{NB} launches back to back on distinct buffers in one graph, per launch",
+                                 "single_launch_ms": round(ms1, 4),
+                                 "single_launch_gbs": round(2 * T * Nn * P * 4 / (ms1 * 1e-3) / 1e9, 1)})
+    del probs, stagings
     rx = torch.empty((Nn, M, H), dtype=torch.bfloat16, device=dev)
     rp = torch.empty((Nn, M, P), dtype=torch.float32, device=dev)
     routed = int(lay.is_token_in_node.sum().item())
@@ -575,7 +758,23 @@ def extra_stages(ep, dev, args, flush, peak):
     ms = time_events(lambda: ep.ep_combine_permuted(px, topk, tw, off, eslot, E, out), n, flush, stream)
     res["combine_permuted_weighted"] = gbs(entries * 2 * H + T * k * 16 + T * 2 * H, ms)
     res["permuted_entries"] = entries
-    del px, ps, pw, d, x, lay, out
+    # split (hook-mode) combine: send phase back into the rank slabs, then the rank combine
+    yr = torch.empty((R, w.max_tokens, H), dtype=torch.bfloat16, device=dev)
+    send = lambda: ep.ep_combine_send(px, d.recv_src_idx, d.recv_topk_idx, d.recv_topk_w, lay.tokens_per_rank, off,
+                                      eslot, E, yr)
+    # read the expert-major rows, each received row's metadata, the expert slots and offsets;
+    # write one rank-level row per received row
+    b_send = entries * 2 * H + pairs * (2 * H + 4 + 8 * k) + T * k * 4 + 4 * (E + 1)
+    ms = time_events(send, n, flush, stream)
+    res["combine_send_weighted"] = gbs(b_send, ms)
+
+    def split():
+        send()
+        ep.combine(yr, lay, w.max_tokens, out=out)
+
+    ms = time_events(split, n, flush, stream)
+    res["split_combine_weighted"] = gbs(b_send + pairs * 2 * H + 4 * T * R + T * 2 * H, ms)
+    del px, ps, pw, d, x, lay, out, yr
 
     # decode-sized batch (T=128 of the same shape): expert layout + dispatch + permute as two
     # launches (one graph) against the single low-latency launch, then the weighted combine
@@ -608,7 +807,31 @@ def extra_stages(ep, dev, args, flush, peak):
     res["decode128_dispatch_permuted_ll"] = gbs(b_dp, ms)
     ms = time_events(lambda: ep.ep_combine_permuted(px, topk, tw, off, eslot, E, out), n, flush, stream)
     res["decode128_combine_permuted_weighted"] = gbs(entries * 2 * H + Td * k * 16 + Td * 2 * H, ms)
+    ms = time_events(lambda: ep.ep_combine_permuted_ll(px, topk, tw, off, eslot, E, out), n, flush, stream)
+    res["decode128_combine_ll_weighted"] = gbs(entries * 2 * H + Td * k * 16 + Td * 2 * H, ms)
+    floor = torch.zeros(4, device=dev)
+    res["event_floor_ms"] = round(time_events(lambda: floor.add_(1), n, flush, stream), 4)
     del px, ps, pw, x, out
+
+    # the tiny workload's whole step (T=128, H=1024, E=16, k=4, R=4), one graph
+    w = workloads.make("tiny")
+    x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(w.topk_idx).to(dev)
+    tw = torch.from_numpy(w.topk_w).to(dev)
+    lay = ep.get_layout(topk, w.E, w.R, w.ranks_per_node)
+    d = ep.alloc_dispatch(w.R, w.max_tokens, w.H, w.k, device=dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+
+    def tiny_step():
+        ep.get_layout(topk, w.E, w.R, w.ranks_per_node, out=lay)
+        ep.dispatch(x, topk, tw, lay, w.max_tokens, out=d)
+        ep.combine(d.recv_x, lay, w.max_tokens, out=out)
+
+    tiny_step()
+    pairs = int(lay.tokens_per_rank.sum().item())
+    ms = time_events(tiny_step, n, flush, stream)
+    res["tiny_step"] = gbs(sum(step_bytes(w.T, w.H, w.k, w.E, w.R, w.num_nodes, pairs).values()), ms)
+    del x, lay, d, out
 
     # skewed routing dispatch + combine (T=16384, H=4096, R=64, max_tokens = hottest rank)
     w = workloads.make("skewed")
@@ -661,7 +884,8 @@ def run_reference(args, world, rank):
         "config": {"workload": "dsv3 prefill: T=4096 H=7168 bf16, E=256 top-8, R=32 virtual ranks "
                                "(8 nodes x 4), max_tokens=4096, identity expert"},
         "tokens_per_s": round(tokens / s, 1),
-        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                         "host": host_cpu()},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -13,6 +13,9 @@ combine, with R virtual EP ranks held as slabs of one GPU's HBM:
   ep_get_expert_layout / ep_dispatch_permuted / ep_permute_received /
   ep_combine_permuted  the expert-major (dispatch + permute) path, fused or split
   ep_dispatch_permuted_ll  the same for a decode-sized batch in one launch
+  ep_combine_send    send phase of a split combine (expert-major rows -> rank slabs);
+                     ep_combine is its receive phase
+  ep_combine_permuted_ll   the expert-major combine shaped for decode-sized batches
 
 The C ABI is include/ep.h (libep_gb300.so, built in-tree by build.py); the
 functions here with the same names are its ctypes binding, and api.py
@@ -24,7 +27,8 @@ from ._lib import (  # noqa: F401
     FLAG_CAPACITY, FLAG_TIMEOUT, FLAG_WORKSPACE, NODES_DENSE, NODES_SPARSE, EpError, ep_combine, ep_dispatch,
     ep_dispatch_nodes, ep_get_layout, ep_get_layout_noalloc, ep_layout_workspace_size, ep_restripe_prob, lib,
     ep_combine_permuted, ep_dispatch_permuted, ep_expert_layout_workspace_size, ep_get_expert_layout,
-    ep_permute_received, ep_combine_fp8, ep_combine_weights, ep_dispatch_permuted_ll,
+    ep_permute_received, ep_combine_fp8, ep_combine_weights, ep_dispatch_permuted_ll, ep_combine_send,
+    ep_combine_permuted_ll,
 )
 from .api import (  # noqa: F401
     Dispatched, Layout, alloc_dispatch, alloc_layout, combine, combine_fp8, combine_weights, dispatch, get_layout,

@@ -40,7 +40,7 @@ EXPORTS = (
     "ep_get_layout", "ep_get_layout_noalloc", "ep_dispatch", "ep_restripe_prob", "ep_dispatch_nodes", "ep_combine",
     "ep_combine_fp8", "ep_combine_weights",
     "ep_expert_layout_workspace_size", "ep_get_expert_layout", "ep_dispatch_permuted", "ep_permute_received",
-    "ep_combine_permuted", "ep_dispatch_permuted_ll",
+    "ep_combine_permuted", "ep_dispatch_permuted_ll", "ep_combine_send", "ep_combine_permuted_ll",
 )
 
 
@@ -92,6 +92,8 @@ def lib():
                     "ep_permute_received": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P,
                                                   P, P]),
                     "ep_combine_permuted": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]),
+                    "ep_combine_permuted_ll": (i32, [P, P, P, P, P, i32, i32, i32, i32, i32, i32, P, P, P]),
+                    "ep_combine_send": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P]),
                 }
                 for name, (res, args) in sigs.items():
                     f = getattr(L, name)
@@ -367,3 +369,46 @@ def ep_dispatch_permuted_ll(x, topk_idx, topk_w, num_experts, num_ranks, max_row
                                        _ptr(perm_w), _ptr(status), _stream(stream))
     _done("ep_dispatch_permuted_ll", rc)
 
+
+
+def ep_combine_permuted_ll(y, topk_idx, topk_w, expert_offsets, expert_slot, num_experts, out, status=None,
+                           stream=None):
+    """ep_combine_permuted for a decode-sized batch (T <= 1024), shaped for latency; same results."""
+    R, max_rows, H = y.shape
+    T, k = topk_idx.shape
+    E = num_experts
+    _check("y", y, torch.bfloat16)
+    _check("topk_idx", topk_idx, torch.int64, (T, k))
+    _check("topk_w", topk_w, torch.float32, (T, k), optional=True)
+    _check("expert_offsets", expert_offsets, torch.int32, (E + 1,))
+    _check("expert_slot", expert_slot, torch.int32, (T, k))
+    _check("out", out, torch.bfloat16, (T, H))
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_combine_permuted_ll(_ptr(y), _ptr(topk_idx), _ptr(topk_w), _ptr(expert_offsets), _ptr(expert_slot),
+                                      T, H, k, E, R, max_rows, _ptr(out), _ptr(status), _stream(stream))
+    _done("ep_combine_permuted_ll", rc)
+
+
+def ep_combine_send(y_perm, recv_src_idx, recv_topk_idx, recv_topk_w, tokens_per_rank, expert_offsets, expert_slot,
+                    num_experts, y_rank, status=None, stream=None):
+    """Send phase of a split combine: expert-major rows reduced back into the rank-level slabs
+    y_rank [R][max_tokens][H], which ep_combine (the receive phase) reads. recv_topk_w None:
+    unweighted."""
+    R, max_rows, H = y_perm.shape
+    M = recv_src_idx.shape[1]
+    k = recv_topk_idx.shape[2]
+    T = expert_slot.shape[0]
+    E = num_experts
+    _check("y_perm", y_perm, torch.bfloat16)
+    _check("recv_src_idx", recv_src_idx, torch.int32, (R, M))
+    _check("recv_topk_idx", recv_topk_idx, torch.int32, (R, M, k))
+    _check("recv_topk_w", recv_topk_w, torch.float32, (R, M, k), optional=True)
+    _check("tokens_per_rank", tokens_per_rank, torch.int32, (R,))
+    _check("expert_offsets", expert_offsets, torch.int32, (E + 1,))
+    _check("expert_slot", expert_slot, torch.int32, (T, k))
+    _check("y_rank", y_rank, torch.bfloat16, (R, M, H))
+    _check("status", status, torch.int32, (1,), optional=True)
+    rc = lib().ep_combine_send(_ptr(y_perm), _ptr(recv_src_idx), _ptr(recv_topk_idx), _ptr(recv_topk_w),
+                               _ptr(tokens_per_rank), _ptr(expert_offsets), _ptr(expert_slot), T, H, k, E, R, M,
+                               max_rows, _ptr(y_rank), _ptr(status), _stream(stream))
+    _done("ep_combine_send", rc)

@@ -707,6 +707,251 @@ __global__ void __launch_bounds__(kThreads, 1) dispatch_permuted_ll_kernel(LLArg
     }
 }
 
+// ---------------------------------------------------------------------------
+// Send phase of a split (hook-mode) combine
+// ---------------------------------------------------------------------------
+
+struct CombineSendArgs {
+    const uint16_t* y_perm;  // [R][max_rows][H]
+    const int32_t* recv_src;
+    const int32_t* recv_tidx;
+    const float* recv_tw;  // nullable: unweighted
+    const int32_t* tokens_per_rank;
+    const int32_t* offsets;
+    const int32_t* eslot;
+    int T, H, k, E, R, max_tokens, max_rows;
+    uint16_t* y_rank;  // [R][max_tokens][H]
+    int32_t* status;
+};
+
+constexpr int kSendGroups = 4;  // 32-vector groups of a row a warp handles at once
+constexpr int kSendBatch = 2;   // sources loaded together
+
+// Warp per received row (r, s), found like permute_received_kernel's rows (prefix of
+// the per-rank counts in shared memory, binary search). Lanes j < k resolve the row's
+// local experts to their expert-major rows, compacted in slot order by a ballot; then the
+// warp walks the row kSendGroups x 32 vectors at a time with up to kSendBatch x
+// kSendGroups source vectors in flight per lane, adding strictly in slot order (one fp32
+// multiply by the row's weight and one fp32 add per term, never fused), and stores one
+// bf16 vector per group, rounded to nearest even.
+__global__ void __launch_bounds__(kThreads) combine_send_kernel(CombineSendArgs a) {
+    grid_dependency_wait();  // dependent launch: the expert outputs are complete after this
+    __shared__ long long s_src[kWarps][kMaxTopk];
+    __shared__ float s_w[kWarps][kMaxTopk];
+    __shared__ int s_base[257];
+    const int lane = lane_id();
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int nvec = a.H / 8;
+    const int epr = a.E / a.R;
+    if (warp == 0) {  // exclusive prefix of the received counts, 32 ranks per step
+        int carry = 0;
+        for (int r0 = 0; r0 < a.R; r0 += 32) {
+            const int r = r0 + lane;
+            int c = 0;
+            if (r < a.R) {
+                c = a.tokens_per_rank[r];
+                c = c < 0 ? 0 : (c < a.max_tokens ? c : a.max_tokens);
+            }
+            int incl = c;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(kFullMask, incl, off);
+                if (lane >= off) incl += v;
+            }
+            if (r < a.R) s_base[r] = carry + incl - c;
+            carry += __shfl_sync(kFullMask, incl, 31);
+        }
+        if (lane == 0) s_base[a.R] = carry;
+    }
+    __syncthreads();
+    const int total = s_base[a.R];
+    const uint4* ys = reinterpret_cast<const uint4*>(a.y_perm);
+    uint4* outs = reinterpret_cast<uint4*>(a.y_rank);
+    for (int q = blockIdx.x * kWarps + warp; q < total; q += gridDim.x * kWarps) {
+        int lo = 0, hi = a.R;  // last r with s_base[r] <= q
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_base[mid] <= q) lo = mid;
+            else hi = mid;
+        }
+        const int r = lo;
+        const size_t row = static_cast<size_t>(r) * a.max_tokens + (q - s_base[r]);
+        const int t = a.recv_src[row];
+        bool ok = false, over = false;
+        long long src = 0;
+        float wj = 1.0f;
+        if (lane < a.k && t >= 0 && t < a.T) {
+            const int l = a.recv_tidx[row * a.k + lane];
+            const int32_t sl = a.eslot[static_cast<size_t>(t) * a.k + lane];
+            if (l >= 0 && l < epr && sl >= 0) {
+                const int p = a.offsets[r * epr + l] - a.offsets[r * epr] + sl;
+                if (p >= 0 && p < a.max_rows) {
+                    ok = true;
+                    src = (static_cast<long long>(r) * a.max_rows + p) * nvec;
+                    if (a.recv_tw != nullptr) wj = a.recv_tw[row * a.k + lane];
+                } else {
+                    over = true;
+                }
+            }
+        }
+        const uint32_t m = __ballot_sync(kFullMask, ok);
+        if (ok) {
+            const int pos = __popc(m & lanemask_lt());
+            s_src[warp][pos] = src;
+            s_w[warp][pos] = wj;
+        }
+        if (__any_sync(kFullMask, over) && lane == 0) raise_flag(a.status, EP_FLAG_CAPACITY);
+        __syncwarp();
+        const int ns = __popc(m);
+        uint4* dst = outs + row * nvec;
+        for (int v0 = lane; v0 < nvec; v0 += 32 * kSendGroups) {
+            float acc[kSendGroups][8];
+#pragma unroll
+            for (int g = 0; g < kSendGroups; ++g)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[g][i] = 0.0f;
+            for (int d0 = 0; d0 < ns; d0 += kSendBatch) {
+                uint4 buf[kSendBatch][kSendGroups];
+#pragma unroll
+                for (int b = 0; b < kSendBatch; ++b)
+#pragma unroll
+                    for (int g = 0; g < kSendGroups; ++g)
+                        if (d0 + b < ns && v0 + 32 * g < nvec) buf[b][g] = ld_stream_v4(ys + s_src[warp][d0 + b] + v0 + 32 * g);
+#pragma unroll
+                for (int b = 0; b < kSendBatch; ++b) {
+                    if (d0 + b >= ns) continue;
+                    const float w = s_w[warp][d0 + b];
+#pragma unroll
+                    for (int g = 0; g < kSendGroups; ++g) {
+                        const uint32_t wd[4] = {buf[b][g].x, buf[b][g].y, buf[b][g].z, buf[b][g].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            if (a.recv_tw != nullptr) {
+                                acc[g][2 * h] = __fadd_rn(acc[g][2 * h], __fmul_rn(bf16_lo(wd[h]), w));
+                                acc[g][2 * h + 1] = __fadd_rn(acc[g][2 * h + 1], __fmul_rn(bf16_hi(wd[h]), w));
+                            } else {
+                                acc[g][2 * h] = __fadd_rn(acc[g][2 * h], bf16_lo(wd[h]));
+                                acc[g][2 * h + 1] = __fadd_rn(acc[g][2 * h + 1], bf16_hi(wd[h]));
+                            }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < kSendGroups; ++g) {
+                if (v0 + 32 * g < nvec) {
+                    uint4 o;
+                    o.x = pack_bf16x2_rn(acc[g][0], acc[g][1]);
+                    o.y = pack_bf16x2_rn(acc[g][2], acc[g][3]);
+                    o.z = pack_bf16x2_rn(acc[g][4], acc[g][5]);
+                    o.w = pack_bf16x2_rn(acc[g][6], acc[g][7]);
+                    st_v4(dst + v0 + 32 * g, o);
+                }
+            }
+        }
+        __syncwarp();
+    }
+    allow_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// Low-latency (decode-sized) combine from expert-major slabs
+// ---------------------------------------------------------------------------
+// The same result as combine_permuted_kernel, shaped for latency: CTA (t, part) handles
+// one token and one slice of at most 256 vectors of its row, a vector per thread. At the
+// start every thread helps to load the expert offsets into shared memory while warp 0
+// loads the token's expert slots, ids and weights, so both reach the CTA in one memory
+// round trip; the rows' positions then come from shared memory, and each thread issues
+// the loads of all of the token's source vectors (kBatch at a time) in a second round
+// trip before adding them in slot order.
+constexpr int kLLCombineVec = kThreads;  // vectors of a row per CTA
+
+__global__ void __launch_bounds__(kThreads) combine_permuted_ll_kernel(CombinePermArgs a, int parts) {
+    grid_dependency_wait();  // dependent launch: the expert outputs are complete after this
+    __shared__ int32_t s_off[kMaxExpertsPerm + 1];
+    __shared__ long long s_src[kMaxTopk];
+    __shared__ float s_w[kMaxTopk];
+    __shared__ int s_ns;
+    const int tid = static_cast<int>(threadIdx.x);
+    const int lane = tid & 31;
+    const int nvec = a.H / 8;
+    const int epr = a.E / a.R;
+    const uint4* ys = reinterpret_cast<const uint4*>(a.y);
+    uint4* os = reinterpret_cast<uint4*>(a.out);
+    for (int b = static_cast<int>(blockIdx.x); b < a.T * parts; b += static_cast<int>(gridDim.x)) {
+        const int t = b / parts;
+        const int v = (b - t * parts) * kLLCombineVec + tid;
+        int32_t sl = -1;
+        int64_t e = -1;
+        float wj = 1.0f;
+        if (tid < a.k) {
+            sl = a.eslot[static_cast<size_t>(t) * a.k + tid];
+            e = a.topk_idx[static_cast<size_t>(t) * a.k + tid];
+            if (a.topk_w != nullptr) wj = a.topk_w[static_cast<size_t>(t) * a.k + tid];
+        }
+        for (int i = tid; i <= a.E; i += kThreads) s_off[i] = a.offsets[i];
+        __syncthreads();
+        if (tid < 32) {
+            bool ok = false, over = false;
+            long long src = 0;
+            if (lane < a.k && sl >= 0 && e >= 0 && e < a.E) {
+                const int r = static_cast<int>(e) / epr;
+                const int p = s_off[e] - s_off[r * epr] + sl;
+                if (p >= 0 && p < a.max_rows) {
+                    ok = true;
+                    src = (static_cast<long long>(r) * a.max_rows + p) * nvec;
+                } else {
+                    over = true;
+                }
+            }
+            const uint32_t m = __ballot_sync(kFullMask, ok);
+            if (ok) {
+                const int pos = __popc(m & lanemask_lt());
+                s_src[pos] = src;
+                s_w[pos] = wj;
+            }
+            if (__any_sync(kFullMask, over) && lane == 0 && b % parts == 0) raise_flag(a.status, EP_FLAG_CAPACITY);
+            if (lane == 0) s_ns = __popc(m);
+        }
+        __syncthreads();
+        const int ns = s_ns;
+        if (v < nvec) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int d0 = 0; d0 < ns; d0 += kBatch) {
+                uint4 buf[kBatch];
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i)
+                    if (d0 + i < ns) buf[i] = ld_stream_v4(ys + s_src[d0 + i] + v);
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i) {
+                    if (d0 + i >= ns) continue;
+                    const uint32_t wd[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
+                    const float w = s_w[d0 + i];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (a.topk_w != nullptr) {
+                            acc[2 * q] = __fadd_rn(acc[2 * q], __fmul_rn(bf16_lo(wd[q]), w));
+                            acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __fmul_rn(bf16_hi(wd[q]), w));
+                        } else {
+                            acc[2 * q] = __fadd_rn(acc[2 * q], bf16_lo(wd[q]));
+                            acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], bf16_hi(wd[q]));
+                        }
+                    }
+                }
+            }
+            uint4 o;
+            o.x = pack_bf16x2_rn(acc[0], acc[1]);
+            o.y = pack_bf16x2_rn(acc[2], acc[3]);
+            o.z = pack_bf16x2_rn(acc[4], acc[5]);
+            o.w = pack_bf16x2_rn(acc[6], acc[7]);
+            st_v4(os + static_cast<size_t>(t) * nvec + v, o);
+        }
+        __syncthreads();  // s_off / s_src / s_ns are rewritten for the next token
+    }
+}
+
+std::atomic<int> g_send_per_sm[kMaxDevices];
+
 std::atomic<int> g_ll_attr_set[kMaxDevices];
 std::atomic<int> g_attr_set[kMaxDevices];
 std::atomic<int> g_combine_per_sm[kMaxDevices];
@@ -854,4 +1099,56 @@ extern "C" ep_status_t ep_dispatch_permuted_ll(const void* x, const int64_t* top
     const int grid = T < 1 ? 1 : (T < sms ? T : sms);
     return launch_dependent(dispatch_permuted_ll_kernel, dim3(grid), dim3(kThreads), ll_smem_bytes(T, k, E),
                             as_stream(stream), a);
+}
+
+extern "C" ep_status_t ep_combine_send(const void* y_perm, const int32_t* recv_src_idx, const int32_t* recv_topk_idx,
+                                       const float* recv_topk_w, const int32_t* tokens_per_rank,
+                                       const int32_t* expert_offsets, const int32_t* expert_slot, int32_t T, int32_t H,
+                                       int32_t k, int32_t E, int32_t R, int32_t max_tokens, int32_t max_rows,
+                                       void* y_rank, int32_t* status, void* stream) {
+    if (!perm_common_ok(T, H, k, E, R, max_rows) || max_tokens < 0 ||
+        static_cast<long long>(R) * max_tokens > 0x7fffffffLL || y_rank == nullptr)
+        return EP_ERR_INVALID;
+    if (T == 0 || max_tokens == 0) return EP_OK;
+    if (recv_src_idx == nullptr || recv_topk_idx == nullptr || tokens_per_rank == nullptr ||
+        expert_offsets == nullptr || expert_slot == nullptr || (max_rows > 0 && y_perm == nullptr))
+        return EP_ERR_INVALID;
+    if (!aligned16_or_null(y_perm) || !aligned16(y_rank) || !aligned16(recv_src_idx) || !aligned16(recv_topk_idx) ||
+        !aligned16_or_null(recv_topk_w) || !aligned16(tokens_per_rank) || !aligned16(expert_offsets) ||
+        !aligned16(expert_slot))
+        return EP_ERR_INVALID;
+    CombineSendArgs a{static_cast<const uint16_t*>(y_perm), recv_src_idx, recv_topk_idx, recv_topk_w, tokens_per_rank,
+                      expert_offsets, expert_slot, T, H, k, E, R, max_tokens, max_rows,
+                      static_cast<uint16_t*>(y_rank), status};
+    int per_sm = 1;
+    const ep_status_t occ = blocks_per_sm(g_send_per_sm, combine_send_kernel, kThreads, 0, &per_sm);
+    if (occ != EP_OK) return occ;
+    // rows received never exceed T per rank nor max_tokens
+    const long long rows = static_cast<long long>(R) * (T < max_tokens ? T : max_tokens);
+    const long long want = (rows + kWarps - 1) / kWarps;
+    const long long cap = static_cast<long long>(sm_count()) * per_sm;
+    const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+    return launch_dependent(combine_send_kernel, dim3(grid), dim3(kThreads), 0, as_stream(stream), a);
+}
+
+extern "C" ep_status_t ep_combine_permuted_ll(const void* y, const int64_t* topk_idx, const float* topk_w,
+                                              const int32_t* expert_offsets, const int32_t* expert_slot, int32_t T,
+                                              int32_t H, int32_t k, int32_t E, int32_t R, int32_t max_rows,
+                                              void* out, int32_t* status, void* stream) {
+    if (!perm_common_ok(T, H, k, E, R, max_rows) || T > kLLMaxTokens || E > kMaxExpertsPerm || out == nullptr)
+        return EP_ERR_INVALID;
+    if (T == 0) return EP_OK;
+    if (topk_idx == nullptr || expert_offsets == nullptr || expert_slot == nullptr || (max_rows > 0 && y == nullptr))
+        return EP_ERR_INVALID;
+    if (!aligned16_or_null(y) || !aligned16(out) || !aligned16(topk_idx) || !aligned16_or_null(topk_w) ||
+        !aligned16(expert_offsets) || !aligned16(expert_slot))
+        return EP_ERR_INVALID;
+    CombinePermArgs a{static_cast<const uint16_t*>(y), topk_idx, topk_w, expert_offsets, expert_slot, T, H, k, E, R,
+                      max_rows, static_cast<uint16_t*>(out), status};
+    const int nvec = H / 8;
+    const int parts = (nvec + kLLCombineVec - 1) / kLLCombineVec;
+    const long long ctas = static_cast<long long>(T) * parts;
+    const long long cap = static_cast<long long>(sm_count()) * 8;
+    const int grid = static_cast<int>(ctas < cap ? ctas : cap);
+    return launch_dependent(combine_permuted_ll_kernel, dim3(grid), dim3(kThreads), 0, as_stream(stream), a, parts);
 }

@@ -386,6 +386,45 @@ ep_status_t ep_combine_permuted(const void* y, const int64_t* topk_idx, const fl
                                 int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
                                 int32_t max_rows, void* out, int32_t* status, void* stream);
 
+/* ep_combine_send -- the send phase of a split ("hook mode", [PR #347] 2.1 Feature: the
+ * send phase runs and returns, the receive phase runs later as its own launch) combine;
+ * the receive phase is ep_combine. It is the inverse of ep_permute_received: every rank
+ * r takes, for each row s < min(tokens_per_rank[r], max_tokens) it received (token
+ * t = recv_src_idx[r][s]), the expert-major rows of the token's local experts -- row
+ * p = expert_offsets[e] - expert_offsets[r*(E/R)] + expert_slot[t][j] for every slot j
+ * with local id l = recv_topk_idx[r][s][j] >= 0, e = r*(E/R) + l -- and reduces them into
+ * its rank-level row:
+ *   y_rank[r][s][h] = bf16_rn(acc), acc = 0; for j = 0 .. k-1 with such a row p:
+ *       acc = acc + recv_topk_w[r][s][j] * float(y_perm[r][p][h])  (weights given: one
+ *                                                                   fp32 multiply, one add)
+ *       acc = acc + float(y_perm[r][p][h])                        (recv_topk_w NULL)
+ * in exactly that order. ep_combine(y_rank, slot, ...) then completes the combine. Each
+ * rank rounds its partial sum to bf16 once (the rank-level rows are bf16, like every
+ * combine input), so the split result can differ from ep_combine_permuted's single fp32
+ * sum in the last bits; it equals it bit for bit when no token has two experts on one
+ * rank, the sum is unweighted and every token's expert ids ascend.
+ *   y_perm bf16 [R][max_rows][H] (H % 8 == 0); recv_src_idx int32 [R][max_tokens],
+ *   recv_topk_idx int32 / recv_topk_w fp32 [R][max_tokens][k] from ep_dispatch;
+ *   tokens_per_rank from ep_get_layout; expert_offsets / expert_slot from
+ *   ep_get_expert_layout; y_rank bf16 [R][max_tokens][H] (other rows not written);
+ *   R * max_rows < 2^31, R * max_tokens < 2^31. p >= max_rows is skipped with
+ *   EP_FLAG_CAPACITY. */
+ep_status_t ep_combine_send(const void* y_perm, const int32_t* recv_src_idx, const int32_t* recv_topk_idx,
+                            const float* recv_topk_w, const int32_t* tokens_per_rank,
+                            const int32_t* expert_offsets, const int32_t* expert_slot, int32_t T,
+                            int32_t H, int32_t k, int32_t E, int32_t R, int32_t max_tokens,
+                            int32_t max_rows, void* y_rank, int32_t* status, void* stream);
+
+/* ep_combine_permuted_ll -- the low-latency (decode-sized) form of ep_combine_permuted
+ * (the pages name low-latency kernels beside the normal ones, [PR #347]): the same
+ * arguments and bit-identical results, for T <= 1024 and E <= 1024, shaped for latency --
+ * one CTA per (token, 256-vector slice of its row), the expert offsets and the token's
+ * slots fetched together, then every source vector of the slice in flight at once. */
+ep_status_t ep_combine_permuted_ll(const void* y, const int64_t* topk_idx, const float* topk_w,
+                                   const int32_t* expert_offsets, const int32_t* expert_slot,
+                                   int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,
+                                   int32_t max_rows, void* out, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

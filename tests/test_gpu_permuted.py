@@ -1,7 +1,9 @@
 """GPU parity of the expert-major path against the oracle, bit for bit: the expert
 layout, the fused dispatch + permute, the receive-side permute of a split dispatch
-(whose result must equal the fused one), and the combine from expert-major slabs,
-weighted and unweighted. Output buffers sit between guard regions."""
+(whose result must equal the fused one), the combine from expert-major slabs (normal
+and low-latency forms), weighted and unweighted, and the split combine (send phase back
+into the rank slabs, then the rank-level combine). Output buffers sit between guard
+regions."""
 import numpy as np
 import pytest
 import torch
@@ -97,6 +99,32 @@ def run_permuted(w, max_rows=None, weighted=True):
         assert int(st3.item()) == flags
         assert np.array_equal(host_bits(out), exp)
         check_guards(bout, out.numel(), SENT_BF16)
+        if T <= 1024 and E <= 1024:  # the low-latency form: the same bits
+            out_ll, bll = guarded((T, H), torch.bfloat16, SENT_BF16)
+            st5 = torch.zeros(1, dtype=torch.int32, device="cuda")
+            ep.ep_combine_permuted_ll(y, topk, wts[0], off, slot, E, out_ll, st5)
+            assert int(st5.item()) == flags
+            assert np.array_equal(host_bits(out_ll), exp)
+            check_guards(bll, out_ll.numel(), SENT_BF16)
+
+    # split combine: send phase (expert-major rows back into the rank slabs), then the
+    # receive phase (the rank-level combine)
+    D = oracle.dispatch(w.x, w.topk_idx, w.topk_w, L["slot"], E, R, Mr, rows=False)
+    for weighted_send in ((True, False) if weighted else (False,)):
+        yr, byr = guarded((R, Mr, H), torch.bfloat16, SENT_BF16)
+        st4 = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ep.ep_combine_send(y, d.recv_src_idx, d.recv_topk_idx, d.recv_topk_w if weighted_send else None,
+                           lay.tokens_per_rank, off, slot, E, yr, st4)
+        exp_r, f_send = oracle.combine_send(y_np, D, L["tokens_per_rank"], EL, T, E, R, weighted=weighted_send,
+                                            fill=SENT_BF16)
+        assert int(st4.item()) == f_send
+        assert np.array_equal(host_bits(yr), exp_r)
+        check_guards(byr, yr.numel(), SENT_BF16)
+        out, bout = guarded((T, H), torch.bfloat16, SENT_BF16)
+        ep.ep_combine(yr, lay.slot, Mr, out)
+        exp_c, _ = oracle.combine(exp_r, L["slot"], Mr)
+        assert np.array_equal(host_bits(out), exp_c)
+        check_guards(bout, out.numel(), SENT_BF16)
 
 
 @pytest.mark.parametrize("name,over", [
@@ -107,6 +135,8 @@ def run_permuted(w, max_rows=None, weighted=True):
     ("skewed", {"T": 3000, "H": 256}),
     ("restripe", {"T": 600, "H": 128}),
     ("dsv3", {"T": 40, "H": 36864}),  # rows too large for the bulk-copy scatter
+    ("dsv3", {"T": 128}),             # a decode batch at the full hidden size
+    ("tiny", {"T": 1000, "H": 8, "k": 32, "E": 64, "R": 4}),  # k = 32: sources in several batches
 ])
 def test_permuted_path_matches_oracle(name, over):
     run_permuted(workloads.make(name, **over))
@@ -228,3 +258,76 @@ def test_low_latency_dispatch_permuted_edge_cases():
     lib = ep.lib()
     assert lib.ep_dispatch_permuted_ll(None, None, None, 1025, 8, 1, 16, 4, 1, None, None, None, None, None, None,
                                        None) == ep.EP_ERR_INVALID
+
+
+def test_split_combine_equals_fused_when_it_must():
+    """Unweighted, one expert per rank per token, ids ascending: the send phase copies rows
+    and the receive phase adds them in the fused combine's order, so the split combine
+    equals ep_combine_permuted bit for bit."""
+    rng = np.random.Generator(np.random.PCG64(12))
+    T, H, E, R, k = 2000, 1024, 64, 64, 8
+    w = workloads.make("tiny", T=T, H=H, E=E, k=k, R=R, ranks_per_node=R)
+    w.topk_idx = np.sort(workloads.routing_uniform(rng, T, E, k), axis=1)
+    topk = torch.from_numpy(w.topk_idx).cuda()
+    EL, off, slot = check_expert_layout(w)
+    Mp = max(1, int(oracle.rows_per_rank(EL["expert_offsets"], E, R).max()))
+    y = dev_bf16(workloads.random_bf16_rows(5, (R, Mp, H)))
+    fused = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine_permuted(y, topk, None, off, slot, E, fused)
+    _, lay = gpu_layout(w)
+    Mr = T
+    d = ep.alloc_dispatch(R, Mr, 8, k)  # only the metadata is needed
+    ep.ep_dispatch(dev_bf16(w.x[:, :8].copy()), ep.DTYPE_BF16, topk, torch.from_numpy(w.topk_w).cuda(), lay.slot, E, R,
+                   Mr, d.recv_x, None, d.recv_src_idx, d.recv_topk_idx, d.recv_topk_w)
+    yr = torch.empty((R, Mr, H), dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine_send(y, d.recv_src_idx, d.recv_topk_idx, None, lay.tokens_per_rank, off, slot, E, yr)
+    split = ep.combine(yr, lay, Mr)
+    assert torch.equal(split, fused)
+
+
+def test_low_latency_combine_edge_cases():
+    """Routed-nowhere tokens (+0 rows), repeated and out-of-range ids, experts with no
+    tokens, capacity drops, the largest batch, an empty batch and the refusals."""
+    w = workloads.make("tiny", T=300, H=64)
+    t = w.topk_idx.copy()
+    t[3, 1] = t[3, 0]   # repeat
+    t[10, 2] = w.E + 5  # out of range
+    t[20, :] = -1       # routed nowhere
+    t[:, :][t == 7] = 6  # expert 7 gets no token
+    t[np.arange(300) % 5 == 0, 3] = -1
+    w.topk_idx = t
+    for over_rows in (None, 0.5):
+        EL = oracle.expert_layout(t, w.E)
+        rows = oracle.rows_per_rank(EL["expert_offsets"], w.E, w.R)
+        M = max(1, int(rows.max())) if over_rows is None else max(1, int(rows.max() * over_rows))
+        y_np = workloads.random_bf16_rows(23, (w.R, M, w.H))
+        off = torch.from_numpy(EL["expert_offsets"]).cuda()
+        slot = torch.from_numpy(EL["expert_slot"]).cuda()
+        for tw_np in (w.topk_w, None):
+            out, bout = guarded((w.T, w.H), torch.bfloat16, SENT_BF16)
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            ep.ep_combine_permuted_ll(dev_bf16(y_np), torch.from_numpy(t).cuda(),
+                                      None if tw_np is None else torch.from_numpy(tw_np).cuda(), off, slot, w.E, out, st)
+            exp, flags = oracle.combine_permuted(y_np, t, tw_np, EL, w.E, w.R)
+            assert int(st.item()) == flags
+            assert np.array_equal(host_bits(out), exp)
+            assert np.all(host_bits(out)[20] == 0)
+            check_guards(bout, out.numel(), SENT_BF16)
+    # the largest batch (T = 1024) at a ragged width
+    w2 = workloads.make("dsv3", T=1024, H=264)
+    EL = oracle.expert_layout(w2.topk_idx, w2.E)
+    Mp = int(oracle.rows_per_rank(EL["expert_offsets"], w2.E, w2.R).max())
+    y_np = workloads.random_bf16_rows(29, (w2.R, Mp, w2.H))
+    out = torch.empty((w2.T, w2.H), dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine_permuted_ll(dev_bf16(y_np), torch.from_numpy(w2.topk_idx).cuda(), torch.from_numpy(w2.topk_w).cuda(),
+                              torch.from_numpy(EL["expert_offsets"]).cuda(), torch.from_numpy(EL["expert_slot"]).cuda(),
+                              w2.E, out)
+    exp, _ = oracle.combine_permuted(y_np, w2.topk_idx, w2.topk_w, EL, w2.E, w2.R)
+    assert np.array_equal(host_bits(out), exp)
+    # empty batch: nothing launched; over the limits: refused before any launch
+    lib = ep.lib()
+    assert lib.ep_combine_permuted_ll(None, None, None, None, None, 0, 8, 4, 16, 4, 1, 4096, None, None) == ep.EP_OK
+    assert lib.ep_combine_permuted_ll(None, None, None, None, None, 1025, 8, 4, 16, 4, 1, 4096, None,
+                                      None) == ep.EP_ERR_INVALID
+    assert lib.ep_combine_permuted_ll(None, None, None, None, None, 8, 8, 4, 2048, 4, 1, 4096, None,
+                                      None) == ep.EP_ERR_INVALID

@@ -95,12 +95,33 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 }
 
 // Combine of FP8 rows (E4M3 codes [R][max_tokens][H], one fp32 scale per 128 channels
-// [R][max_tokens][H/128]): as combine_kernel, with items of (token, 32 lanes x 16
-// channels); a lane loads 16 codes (one 16-byte vector) and its block's scale per source
-// row, converts the codes to fp32 exactly (E4M3 -> fp16 -> fp32), and adds
-// __fmul_rn(code, scale) to its accumulators, source rows in ascending rank order. (The
-// arithmetic stays scalar: a packed .f32x2 multiply feeding a packed add is contracted
-// into a fused multiply-add by the code generator, one rounding instead of two.)
+// [R][max_tokens][H/128]). Items are (token, 32 lanes x 16 channels); each warp takes a
+// contiguous run of its CTA's items, so consecutive items mostly belong to one token and
+// the token's compacted source list (ascending rank) is built once and reused. Per item a
+// lane loads, for kBatchFp8 sources at a time, 16 codes (one 16-byte vector) and its
+// block's scale, converts the codes to fp32 exactly (E4M3 -> fp16 -> fp32 through 16-bit
+// register halves) and adds __fmul_rn(code, scale) to its accumulators in source order.
+// The first term is taken as fma(code, scale, +0) = RN(code * scale + 0), one instruction
+// instead of two. It equals 0 + RN(code * scale) unless a nonzero product rounds to zero
+// (the fused form would keep a -0): with |code| >= 2^-9 that needs a scale below 2^-140,
+// so such scales (never produced by real data) take the two-instruction form.
+// (The arithmetic stays scalar: a packed .f32x2 multiply feeding a packed add is
+// contracted into a fused multiply-add by the code generator, one rounding instead of two.)
+template <bool kFirst>
+__device__ __forceinline__ void fp8_term16(float* acc, const uint4& v, float sc) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        float f[4];
+        ep::e4m3x4_to_f32(w[q], f[0], f[1], f[2], f[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            acc[4 * q + i] = kFirst ? __fmaf_rn(f[i], sc, 0.0f) : __fadd_rn(acc[4 * q + i], __fmul_rn(f[i], sc));
+    }
+}
+
+__device__ __forceinline__ bool fused_first_ok(float sc) { return sc == 0.0f || sc >= 0x1p-140f; }
+
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
     combine_fp8_kernel(const uint8_t* __restrict__ y, const float* __restrict__ y_scales,
                        const int32_t* __restrict__ slot, int T, int H, int R, int max_tokens,
@@ -113,61 +134,59 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     const int nblk = H / 128;
     const int ngroups = (nvec + 31) / 32;
     const long long items = static_cast<long long>(T) * ngroups;
-    const long long i0 = static_cast<long long>(blockIdx.x) * items / gridDim.x;
-    const long long i1 = static_cast<long long>(blockIdx.x + 1) * items / gridDim.x;
+    const long long c0 = static_cast<long long>(blockIdx.x) * items / gridDim.x;
+    const long long c1 = static_cast<long long>(blockIdx.x + 1) * items / gridDim.x;
+    const long long i0 = c0 + (c1 - c0) * warp / kWarps;  // this warp's contiguous run
+    const long long i1 = c0 + (c1 - c0) * (warp + 1) / kWarps;
     const uint4* ys = reinterpret_cast<const uint4*>(y);
     uint4* os = reinterpret_cast<uint4*>(out);
 
-    for (long long it = i0 + warp; it < i1; it += kWarps) {
+    int t_cur = -1, ns = 0;
+    for (long long it = i0; it < i1; ++it) {
         const int t = static_cast<int>(it / ngroups);
         const int v = static_cast<int>(it - static_cast<long long>(t) * ngroups) * 32 + lane;
-        int ns = 0;
-        bool over_any = false;
-        for (int r0 = 0; r0 < R; r0 += 32) {
-            const int r = r0 + lane;
-            const int s = r < R ? slot[static_cast<size_t>(t) * R + r] : -1;
-            const bool over = s >= max_tokens;
-            over_any |= over;
-            const bool ok = s >= 0 && !over;
-            const uint32_t m = __ballot_sync(ep::kFullMask, ok);
-            if (ok) s_src[warp][ns + __popc(m & ep::lanemask_lt())] = static_cast<long long>(r) * max_tokens + s;
-            ns += __popc(m);
+        if (t != t_cur) {  // the token's sources, ascending rank
+            t_cur = t;
+            ns = 0;
+            bool over_any = false;
+            __syncwarp();
+            for (int r0 = 0; r0 < R; r0 += 32) {
+                const int r = r0 + lane;
+                const int s = r < R ? slot[static_cast<size_t>(t) * R + r] : -1;
+                const bool over = s >= max_tokens;
+                over_any |= over;
+                const bool ok = s >= 0 && !over;
+                const uint32_t m = __ballot_sync(ep::kFullMask, ok);
+                if (ok) s_src[warp][ns + __popc(m & ep::lanemask_lt())] = static_cast<long long>(r) * max_tokens + s;
+                ns += __popc(m);
+            }
+            // one report per token: the warp whose run holds the token's first item
+            if (__any_sync(ep::kFullMask, over_any) && lane == 0 && v < 32) ep::raise_flag(status, EP_FLAG_CAPACITY);
+            __syncwarp();
         }
-        if (over_any && v == lane) ep::raise_flag(status, EP_FLAG_CAPACITY);
-        __syncwarp();
 
         float acc[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
         const int blk = v / 8;  // the lane's 16 channels lie in block v / 8
-        for (int d0 = 0; d0 < ns; d0 += kBatchFp8) {
-            uint4 buf[kBatchFp8];
-            float sc[kBatchFp8];
+        if (v < nvec) {
+            for (int d0 = 0; d0 < ns; d0 += kBatchFp8) {
+                uint4 buf[kBatchFp8];
+                float sc[kBatchFp8];
 #pragma unroll
-            for (int i = 0; i < kBatchFp8; ++i) {
-                if (d0 + i < ns && v < nvec) {
-                    const long long row = s_src[warp][d0 + i];
-                    buf[i] = ep::ld_stream_v4(ys + row * nvec + v);
-                    sc[i] = __ldg(y_scales + row * nblk + blk);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < kBatchFp8; ++i) {
-                if (d0 + i < ns) {
-                    const uint32_t w[4] = {buf[i].x, buf[i].y, buf[i].z, buf[i].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint32_t a = ep::e4m3x2_to_f16x2(w[q] & 0xffffu);
-                        const uint32_t b = ep::e4m3x2_to_f16x2(w[q] >> 16);
-                        acc[4 * q + 0] = __fadd_rn(acc[4 * q + 0], __fmul_rn(ep::f16_to_f32(a & 0xffffu), sc[i]));
-                        acc[4 * q + 1] = __fadd_rn(acc[4 * q + 1], __fmul_rn(ep::f16_to_f32(a >> 16), sc[i]));
-                        acc[4 * q + 2] = __fadd_rn(acc[4 * q + 2], __fmul_rn(ep::f16_to_f32(b & 0xffffu), sc[i]));
-                        acc[4 * q + 3] = __fadd_rn(acc[4 * q + 3], __fmul_rn(ep::f16_to_f32(b >> 16), sc[i]));
+                for (int i = 0; i < kBatchFp8; ++i) {
+                    if (d0 + i < ns) {
+                        const long long row = s_src[warp][d0 + i];
+                        buf[i] = ep::ld_stream_v4(ys + row * nvec + v);
+                        sc[i] = __ldg(y_scales + row * nblk + blk);
                     }
                 }
+                if (d0 == 0 && fused_first_ok(sc[0])) fp8_term16<true>(acc, buf[0], sc[0]);
+                else fp8_term16<false>(acc, buf[0], sc[0]);
+#pragma unroll
+                for (int i = 1; i < kBatchFp8; ++i)
+                    if (d0 + i < ns) fp8_term16<false>(acc, buf[i], sc[i]);
             }
-        }
-        if (v < nvec) {
             uint4 o0, o1;
             o0.x = ep::pack_bf16x2_rn(acc[0], acc[1]);
             o0.y = ep::pack_bf16x2_rn(acc[2], acc[3]);
@@ -181,7 +200,6 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
             ep::st_v4(dst, o0);
             ep::st_v4(dst + 1, o1);
         }
-        __syncwarp();
     }
 }
 

@@ -232,6 +232,21 @@ __device__ __forceinline__ uint32_t pack_e4m3x2_rn_sat(float lo, float hi) {
     return r;
 }
 
+// four fp32 -> four OCP E4M3 codes (a in byte 0 ... d in byte 3), each rounded to nearest
+// even and saturated to +-448
+__device__ __forceinline__ uint32_t pack_e4m3x4_rn_sat(float a, float b, float c, float d) {
+    uint32_t r;
+    asm("{\n"
+        " .reg .b16 lo, hi;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+        " mov.b32 %0, {lo, hi};\n"
+        "}"
+        : "=r"(r)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+
 // two OCP E4M3 codes (byte 0 -> low half, byte 1 -> high half) -> two fp16, exactly
 // (every E4M3 value is an fp16 value); then fp16 -> fp32, exactly
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
@@ -239,6 +254,26 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     const uint16_t c = static_cast<uint16_t>(two_codes);
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
     return r;
+}
+// four OCP E4M3 codes (byte i of w) -> four fp32 values, exactly: each 16-bit half of w
+// becomes an fp16 pair (every E4M3 value is an fp16 value) and each fp16 an fp32; the
+// halves are named as 16-bit registers so no masking or shifting is needed
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float& a, float& b, float& c, float& d) {
+    asm("{\n"
+        " .reg .b16 c0, c1, f0, f1, f2, f3;\n"
+        " .reg .b32 h01, h23;\n"
+        " mov.b32 {c0, c1}, %4;\n"
+        " cvt.rn.f16x2.e4m3x2 h01, c0;\n"
+        " cvt.rn.f16x2.e4m3x2 h23, c1;\n"
+        " mov.b32 {f0, f1}, h01;\n"
+        " mov.b32 {f2, f3}, h23;\n"
+        " cvt.f32.f16 %0, f0;\n"
+        " cvt.f32.f16 %1, f1;\n"
+        " cvt.f32.f16 %2, f2;\n"
+        " cvt.f32.f16 %3, f3;\n"
+        "}"
+        : "=f"(a), "=f"(b), "=f"(c), "=f"(d)
+        : "r"(w));
 }
 __device__ __forceinline__ float f16_to_f32(uint32_t h) {
     float f;

@@ -141,22 +141,28 @@ __global__ void __launch_bounds__(kThreads, 2) dispatch_bf16_kernel(DispatchArgs
     }
 }
 
-// x / scale, correctly rounded to fp32, as far as its E4M3 rounding can tell. The
-// E4M3 code of a quotient only changes where the quotient crosses a midpoint
-// between two E4M3 values. y = x * RN(1/scale) is within 3 ulp of RN(x / scale)
-// (three roundings -- of 1/scale, of the product, of the exact quotient -- each at
-// most half an ulp of relative error, and an ulp is at least 2^-24 of the value),
-// so whenever y is
-// more than 8 ulp away from every midpoint the two quotients round to the same
-// code and y is used. For a normal E4M3 binade the midpoints are the fp32 values
-// whose 20 mantissa bits below the 3 E4M3 mantissa bits read 0x80000; below 2^-6
-// (the E4M3 subnormals) and near a midpoint the exact division decides.
+// x / scale correctly rounded to fp32, for a normal scale. The quotient is the product by
+// the correctly rounded reciprocal, corrected once by its residual (Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34,
+// 1990): with rcp = RN(1/scale) and q0 = RN(x * rcp) within an ulp of x / scale, the
+// residual x - q0 * scale is exact in one fused multiply-add and q0 + rcp * residual,
+// rounded once, is RN(x / scale). Quotients that fall below the fp32 normal range only
+// ever round to an E4M3 zero, whose sign is the sign of x; the correction turns a zero x
+// into +0, so x's sign bit is put back (for every other x it is already there).
 __device__ __forceinline__ float quotient(float x, float scale, float rcp) {
-    const float y = __fmul_rn(x, rcp);
-    const uint32_t b = __float_as_uint(y) & 0x7fffffffu;
-    const uint32_t low = b & 0xfffffu;
-    const bool near_midpoint = low - 0x7fff8u < 16u;
-    return (b < 0x3c800000u || near_midpoint) ? __fdiv_rn(x, scale) : y;
+    const float q0 = __fmul_rn(x, rcp);
+    const float e = __fmaf_rn(-q0, scale, x);
+    const float q1 = __fmaf_rn(e, rcp, q0);
+    return __uint_as_float(__float_as_uint(q1) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// amax / 448 correctly rounded: the same correction with RN(1/448), valid while the
+// quotient is a normal fp32 (amax >= 2^-116); smaller amax take the IEEE division
+__device__ __forceinline__ float scale_of(float amax) {
+    constexpr float kInv448 = 1.0f / 448.0f;  // correctly rounded at compile time
+    if (amax < 0x1p-116f) return __fdiv_rn(amax, 448.0f);
+    const float q0 = __fmul_rn(amax, kInv448);
+    return __fmaf_rn(__fmaf_rn(-q0, 448.0f, amax), kInv448, q0);
 }
 
 // bf16 dispatch through the shared bulk-copy scatter (ep_scatter.cuh): source row t is
@@ -194,28 +200,35 @@ __device__ __forceinline__ void quantize16(const uint4& a, const uint4& b, uint4
     // max over the 8 lanes of this block (xor offsets < 8 stay in the group)
 #pragma unroll
     for (int off = 4; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(ep::kFullMask, amax, off));
-    scale = __fdiv_rn(amax, 448.0f);
-    uint32_t c[8];
+    scale = scale_of(amax);
     if (amax == 0.0f) {
         // all elements are +-0: keep the sign of each zero
+        uint32_t c[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            c[i] = ((__float_as_uint(f[2 * i]) >> 31) ? 0x80u : 0u) |
-                   ((__float_as_uint(f[2 * i + 1]) >> 31) ? 0x8000u : 0u);
-    } else if (scale >= 1.17549435e-38f) {  // 1/scale is finite: quotient by multiplication
+        for (int i = 0; i < 4; ++i)
+            c[i] = (__float_as_uint(f[4 * i]) >> 31) << 7 | (__float_as_uint(f[4 * i + 1]) >> 31) << 15 |
+                   (__float_as_uint(f[4 * i + 2]) >> 31) << 23 | (__float_as_uint(f[4 * i + 3]) >> 31) << 31;
+        q = make_uint4(c[0], c[1], c[2], c[3]);
+    } else if (scale >= 1.17549435e-38f) {  // 1/scale is finite: the corrected product
         const float rcp = __frcp_rn(scale);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            c[i] = ep::pack_e4m3x2_rn_sat(quotient(f[2 * i], scale, rcp), quotient(f[2 * i + 1], scale, rcp));
+        q.x = ep::pack_e4m3x4_rn_sat(quotient(f[0], scale, rcp), quotient(f[1], scale, rcp),
+                                     quotient(f[2], scale, rcp), quotient(f[3], scale, rcp));
+        q.y = ep::pack_e4m3x4_rn_sat(quotient(f[4], scale, rcp), quotient(f[5], scale, rcp),
+                                     quotient(f[6], scale, rcp), quotient(f[7], scale, rcp));
+        q.z = ep::pack_e4m3x4_rn_sat(quotient(f[8], scale, rcp), quotient(f[9], scale, rcp),
+                                     quotient(f[10], scale, rcp), quotient(f[11], scale, rcp));
+        q.w = ep::pack_e4m3x4_rn_sat(quotient(f[12], scale, rcp), quotient(f[13], scale, rcp),
+                                     quotient(f[14], scale, rcp), quotient(f[15], scale, rcp));
     } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            c[i] = ep::pack_e4m3x2_rn_sat(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+        q.x = ep::pack_e4m3x4_rn_sat(__fdiv_rn(f[0], scale), __fdiv_rn(f[1], scale), __fdiv_rn(f[2], scale),
+                                     __fdiv_rn(f[3], scale));
+        q.y = ep::pack_e4m3x4_rn_sat(__fdiv_rn(f[4], scale), __fdiv_rn(f[5], scale), __fdiv_rn(f[6], scale),
+                                     __fdiv_rn(f[7], scale));
+        q.z = ep::pack_e4m3x4_rn_sat(__fdiv_rn(f[8], scale), __fdiv_rn(f[9], scale), __fdiv_rn(f[10], scale),
+                                     __fdiv_rn(f[11], scale));
+        q.w = ep::pack_e4m3x4_rn_sat(__fdiv_rn(f[12], scale), __fdiv_rn(f[13], scale), __fdiv_rn(f[14], scale),
+                                     __fdiv_rn(f[15], scale));
     }
-    q.x = c[0] | (c[1] << 16);
-    q.y = c[2] | (c[3] << 16);
-    q.z = c[4] | (c[5] << 16);
-    q.w = c[6] | (c[7] << 16);
 }
 
 // FP8 dispatch: a warp iteration covers 4 blocks (512 elements); lane l owns

@@ -243,7 +243,8 @@ def test_expert_layout_multi_wave_grid_matches_oracle():
 
 def test_fp8_ties_subnormals_and_signed_zeros():
     """Blocks with amax = 448 (scale exactly 1) whose other elements sit on E4M3 midpoints
-    (normal and subnormal), plus an all-zero block with -0 entries."""
+    (normal and subnormal), an all-zero block with -0 entries, and +-0 entries inside
+    blocks whose amax is not zero (E4M3 codes 0x00 / 0x80)."""
     mids = []
     vals = sorted({oracle.e4m3_to_f32(c) for c in range(0x7F) if c != 0x7F})
     for a, b in zip(vals[:-1], vals[1:]):
@@ -260,6 +261,9 @@ def test_fp8_ties_subnormals_and_signed_zeros():
         if i == 3:
             blocks[2] = np.zeros(128, np.float32)
             blocks[2][::3] = -0.0
+        if i == 4:  # signed zeros inside blocks whose amax is not zero
+            blocks[1][::5] = -0.0
+            blocks[3][1::7] = 0.0
         rows.append(np.concatenate(blocks))
     xf = np.stack(rows).astype(np.float32)
     bits = workloads.bf16_bits(xf)

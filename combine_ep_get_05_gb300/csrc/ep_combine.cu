@@ -142,9 +142,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
     uint4* os = reinterpret_cast<uint4*>(out);
 
     int t_cur = -1, ns = 0;
+    // (token, group) of the run's first item; later items advance it without dividing
+    int t = static_cast<int>(i0 / ngroups);
+    int g = static_cast<int>(i0 - static_cast<long long>(t) * ngroups);
     for (long long it = i0; it < i1; ++it) {
-        const int t = static_cast<int>(it / ngroups);
-        const int v = static_cast<int>(it - static_cast<long long>(t) * ngroups) * 32 + lane;
+        const int v = g * 32 + lane;
         if (t != t_cur) {  // the token's sources, ascending rank
             t_cur = t;
             ns = 0;
@@ -199,6 +201,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
             uint4* dst = os + (static_cast<size_t>(t) * nvec + v) * 2;
             ep::st_v4(dst, o0);
             ep::st_v4(dst + 1, o1);
+        }
+        if (++g == ngroups) {
+            g = 0;
+            ++t;
         }
     }
 }

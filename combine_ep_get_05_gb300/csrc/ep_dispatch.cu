@@ -231,20 +231,26 @@ __device__ __forceinline__ void quantize16(const uint4& a, const uint4& b, uint4
     }
 }
 
-// FP8 dispatch: a warp iteration covers 4 blocks (512 elements); lane l owns
-// elements 16*(l % 8) .. +15 of block l / 8, so every code store is one 16-byte
-// vector per lane (512 bytes per warp instruction) and the 4 scales of an
-// iteration leave in one 16-byte store when they are 16-byte aligned.
+// FP8 dispatch: a warp iteration covers 4 blocks (512 elements); lane l owns elements
+// 16*(l % 8) .. +15 of block l / 8, so every code store is one 16-byte vector per lane
+// (512 bytes per warp instruction). The block scales of a token (up to kScaleRow blocks,
+// H <= 32768) are gathered in shared memory and each destination's scale row is written
+// once per token, 16 bytes per lane when the row is 16-byte aligned -- instead of one
+// single-lane 16-byte store per destination and iteration, which made half of all store
+// instructions.
+constexpr int kScaleRow = 256;
+
 __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a, int interleave) {
     ep::grid_dependency_wait();  // dependent launch: inputs are ready after this
     __shared__ int s_rank[kWarps][kMaxDest];
     __shared__ long long s_row[kWarps][kMaxDest];
+    __shared__ __align__(16) float s_sc[kWarps][kScaleRow];
     const int lane = ep::lane_id();
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int nblk = a.H / 128;
     const int grp = lane >> 3;  // block of the iteration this lane works on (0..3)
     const int pos = lane & 7;   // 16-element slice within the block
-    const bool vec_scales = (nblk & 3) == 0;
+    const bool row_scales = nblk <= kScaleRow;
     uint8_t* recv = static_cast<uint8_t*>(a.recv_x);
 
     // one wave: token c + G*w goes to warp w of CTA c, so every SM gets the same number of
@@ -269,30 +275,35 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a, 
             }
             uint4 q[kUnrollFp8];
             float sc[kUnrollFp8];
-            float4 sc4[kUnrollFp8];
 #pragma unroll
             for (int u = 0; u < kUnrollFp8; ++u) {
                 quantize16(lo[u], hi[u], q[u], sc[u]);
-                sc4[u].x = __shfl_sync(ep::kFullMask, sc[u], 0);
-                sc4[u].y = __shfl_sync(ep::kFullMask, sc[u], 8);
-                sc4[u].z = __shfl_sync(ep::kFullMask, sc[u], 16);
-                sc4[u].w = __shfl_sync(ep::kFullMask, sc[u], 24);
+                const int b = b0 + 4 * u + grp;
+                if (row_scales && pos == 0 && b < nblk) s_sc[warp][b] = sc[u];
             }
             for (int d = 0; d < nd; ++d) {
                 const size_t row = static_cast<size_t>(s_row[warp][d]);
                 uint8_t* dst = recv + row * a.H;
-                float* dsc = a.recv_scales + row * nblk;
 #pragma unroll
                 for (int u = 0; u < kUnrollFp8; ++u) {
                     const int b = b0 + 4 * u + grp;
-                    if (b < nblk) ep::st_v4(dst + b * 128 + pos * 16, q[u]);
-                    if (vec_scales) {
-                        if (lane == 0 && b0 + 4 * u < nblk) ep::st_v4(dsc + b0 + 4 * u, make_uint4(
-                            __float_as_uint(sc4[u].x), __float_as_uint(sc4[u].y), __float_as_uint(sc4[u].z),
-                            __float_as_uint(sc4[u].w)));
-                    } else if (pos == 0 && b < nblk) {
-                        dsc[b] = sc[u];
+                    if (b < nblk) {
+                        ep::st_v4(dst + b * 128 + pos * 16, q[u]);
+                        if (!row_scales && pos == 0) a.recv_scales[row * nblk + b] = sc[u];
                     }
+                }
+            }
+        }
+        if (row_scales) {  // the token's scale row to every destination
+            __syncwarp();
+            const bool vec = (nblk & 3) == 0;
+            for (int d = 0; d < nd; ++d) {
+                float* dsc = a.recv_scales + static_cast<size_t>(s_row[warp][d]) * nblk;
+                if (vec) {
+                    for (int i = lane; i < nblk / 4; i += 32)
+                        ep::st_v4(dsc + 4 * i, *reinterpret_cast<const uint4*>(&s_sc[warp][4 * i]));
+                } else {
+                    for (int i = lane; i < nblk; i += 32) dsc[i] = s_sc[warp][i];
                 }
             }
         }

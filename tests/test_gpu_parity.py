@@ -101,6 +101,7 @@ def run_rank_path(w, max_tokens=None, full_compare=True):
     ("dsv3_fp8", {"T": 333, "H": 384}),
     ("dsv3_fp8", {"T": 300, "H": 24576}),  # wide FP8 rows
     ("dsv3_fp8", {"T": 40, "H": 26624}),
+    ("dsv3_fp8", {"T": 30, "H": 33024}),   # more than 256 blocks: scales stored per iteration
     ("dsv3", {"T": 40, "H": 36864}),       # bf16 rows too large for the bulk-copy scatter
     ("skewed", {"T": 2000, "H": 256}),
     ("restripe", {"T": 700, "H": 512}),

@@ -809,6 +809,22 @@ def extra_stages(ep, dev, args, flush, peak):
     res["decode128_combine_permuted_weighted"] = gbs(entries * 2 * H + Td * k * 16 + Td * 2 * H, ms)
     ms = time_events(lambda: ep.ep_combine_permuted_ll(px, topk, tw, off, eslot, E, out), n, flush, stream)
     res["decode128_combine_ll_weighted"] = gbs(entries * 2 * H + Td * k * 16 + Td * 2 * H, ms)
+    # the decode round trip (dispatch + permute, then the weighted combine of the permuted
+    # rows as the identity expert's output), in one graph: the normal kernels (expert layout,
+    # dispatch + permute, combine) against the two low-latency launches, whose combine is
+    # scheduled while the dispatch still runs
+    b_rt = b_dp + entries * 2 * H + Td * k * 16 + Td * 2 * H
+
+    def normal_rt():
+        two_launches()
+        ep.ep_combine_permuted(px, topk, tw, off, eslot, E, out)
+
+    def ll_rt():
+        ep.ep_dispatch_permuted_ll(x, topk, tw, E, R, Mp, off, eslot, px, ps, pw)
+        ep.ep_combine_permuted_ll(px, topk, tw, off, eslot, E, out)
+
+    res["decode128_roundtrip_normal"] = gbs(b_rt, time_events(normal_rt, n, flush, stream))
+    res["decode128_roundtrip_ll"] = gbs(b_rt, time_events(ll_rt, n, flush, stream))
     floor = torch.zeros(4, device=dev)
     res["event_floor_ms"] = round(time_events(lambda: floor.add_(1), n, flush, stream), 4)
     del px, ps, pw, x, out

@@ -532,6 +532,10 @@ inline size_t ll_smem_bytes(int T, int k, int E) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) dispatch_permuted_ll_kernel(LLArgs a) {
+    // a decode batch's grid leaves most of every SM free: the next kernel (the expert work,
+    // or the low-latency combine launched as a dependent launch) may settle its CTAs now and
+    // wait on the device for this grid, so its launch latency is hidden behind this one
+    allow_dependents();
     grid_dependency_wait();  // dependent launch: inputs are ready after this
     extern __shared__ uint32_t smem[];
     uint32_t* s_emask = smem;                                              // [kWarps][E]
@@ -726,6 +730,7 @@ struct CombineSendArgs {
 
 constexpr int kSendGroups = 4;  // 32-vector groups of a row a warp handles at once
 constexpr int kSendBatch = 2;   // sources loaded together
+constexpr int kSendWide = 8;    // groups in flight for a row with a single source
 
 // Warp per received row (r, s), found like permute_received_kernel's rows (prefix of
 // the per-rank counts in shared memory, binary search). Lanes j < k resolve the row's
@@ -733,7 +738,8 @@ constexpr int kSendBatch = 2;   // sources loaded together
 // warp walks the row kSendGroups x 32 vectors at a time with up to kSendBatch x
 // kSendGroups source vectors in flight per lane, adding strictly in slot order (one fp32
 // multiply by the row's weight and one fp32 add per term, never fused), and stores one
-// bf16 vector per group, rounded to nearest even.
+// bf16 vector per group, rounded to nearest even. A row with a single local expert (most
+// rows) keeps kSendWide groups of loads in flight and computes 0 + term per channel.
 __global__ void __launch_bounds__(kThreads) combine_send_kernel(CombineSendArgs a) {
     grid_dependency_wait();  // dependent launch: the expert outputs are complete after this
     __shared__ long long s_src[kWarps][kMaxTopk];
@@ -804,6 +810,32 @@ __global__ void __launch_bounds__(kThreads) combine_send_kernel(CombineSendArgs 
         __syncwarp();
         const int ns = __popc(m);
         uint4* dst = outs + row * nvec;
+        if (ns == 1) {
+            // one local expert (most rows): acc = 0 + term, kSendWide groups of loads in flight
+            const uint4* src1 = ys + s_src[warp][0];
+            const float w = s_w[warp][0];
+            for (int v0 = lane; v0 < nvec; v0 += 32 * kSendWide) {
+                uint4 buf[kSendWide];
+#pragma unroll
+                for (int g = 0; g < kSendWide; ++g)
+                    if (v0 + 32 * g < nvec) buf[g] = ld_stream_v4(src1 + v0 + 32 * g);
+#pragma unroll
+                for (int g = 0; g < kSendWide; ++g) {
+                    if (v0 + 32 * g >= nvec) continue;
+                    const uint32_t wd[4] = {buf[g].x, buf[g].y, buf[g].z, buf[g].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float lo = a.recv_tw != nullptr ? __fmul_rn(bf16_lo(wd[h]), w) : bf16_lo(wd[h]);
+                        const float hi = a.recv_tw != nullptr ? __fmul_rn(bf16_hi(wd[h]), w) : bf16_hi(wd[h]);
+                        o[h] = pack_bf16x2_rn(__fadd_rn(0.0f, lo), __fadd_rn(0.0f, hi));
+                    }
+                    st_v4(dst + v0 + 32 * g, make_uint4(o[0], o[1], o[2], o[3]));
+                }
+            }
+            __syncwarp();
+            continue;
+        }
         for (int v0 = lane; v0 < nvec; v0 += 32 * kSendGroups) {
             float acc[kSendGroups][8];
 #pragma unroll

@@ -88,8 +88,10 @@ def run_permuted(w, max_rows=None, weighted=True):
     for b, v, f in ((bsx, sx, SENT_BF16), (bss, ss, SENT_I32), (bsw, sw, SENT_F32)):
         check_guards(b, v.numel(), f)
 
-    # combine from the slabs: random expert outputs (seeded), weighted and plain
+    # combine from the slabs: random expert outputs (seeded), weighted and plain; some
+    # entries are -0 (a sum that starts from +0 turns a lone -0 term into +0)
     y_np = workloads.random_bf16_rows(17, (R, M, H))
+    y_np.reshape(-1)[::97] = 0x8000
     y = dev_bf16(y_np)
     for wts in (((tw, w.topk_w),) if weighted else ()) + ((None, None),):
         out, bout = guarded((T, H), torch.bfloat16, SENT_BF16)

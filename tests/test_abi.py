@@ -118,3 +118,53 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     with pytest.raises((RuntimeError, ValueError)):
         L.ep_combine(torch.zeros((2, 1, 8), dtype=torch.bfloat16), torch.zeros((1, 2), dtype=torch.int32), 1,
                      torch.zeros((1, 8), dtype=torch.bfloat16))
+
+
+def test_entry_points_from_several_host_threads(libep):
+    """Several host threads entering the library at once: 8 threads x 100 rounds of
+    argument checks that must all be refused (EP_ERR_INVALID, nothing launched) and, on a
+    machine without a GPU, of well-formed calls that reach the CUDA runtime first (the
+    per-device caches, then EP_ERR_CUDA) -- each thread then reads its own nonzero
+    ep_last_cuda_error, which a refused call leaves unchanged."""
+    import threading
+
+    import torch
+
+    L, _ = libep
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: every call below stops before a launch
+    null = None
+    reach_cuda = not torch.cuda.is_available()  # with a GPU these shapes would launch
+    errors = []
+
+    def worker(i):
+        try:
+            for _ in range(100):
+                assert L.ep_dispatch(fake, 0, fake, fake, fake, 16, 7, 4, 16, 4, 16, fake, null, null, null, null,
+                                     null, null) == 1
+                assert L.ep_combine(fake, fake, 16, 64, 4, 16, P(4096 + 4), null, null) == 1
+                assert L.ep_restripe_prob(fake, 17, 8, 8, 16, fake, null) == 1
+                assert L.ep_combine_permuted_ll(null, null, null, null, null, 1025, 8, 4, 16, 4, 1, fake, null,
+                                                null) == 1
+                if reach_cuda:
+                    for rc in (L.ep_combine(fake, fake, 16, 64, 4, 16, fake, null, null),
+                               L.ep_combine_fp8(fake, fake, fake, 16, 128, 4, 16, fake, null, null),
+                               L.ep_dispatch(fake, 1, fake, fake, fake, 16, 128, 4, 16, 4, 16, fake, fake, null, null,
+                                             null, null, null),
+                               L.ep_restripe_prob(fake, 16, 8, 8, 16, fake, null),
+                               L.ep_get_layout(fake, 16, 4, 16, 4, 0, fake, fake, null, fake, null, fake, fake,
+                                               1 << 20, null, null)):
+                        assert rc == 2, rc
+                        assert L.ep_last_cuda_error() != 0
+                    code = L.ep_last_cuda_error()
+                    assert L.ep_combine(fake, fake, 16, 64, 4, 16, P(4096 + 4), null, null) == 1
+                    assert L.ep_last_cuda_error() == code  # a refused call records nothing
+        except Exception as e:  # collected for the main thread
+            errors.append((i, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[:3]

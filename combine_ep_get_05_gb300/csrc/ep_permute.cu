@@ -731,17 +731,103 @@ struct CombineSendArgs {
 constexpr int kSendGroups = 4;  // 32-vector groups of a row a warp handles at once
 constexpr int kSendBatch = 2;   // sources loaded together
 constexpr int kSendWide = 8;    // groups in flight for a row with a single source
+constexpr int kSendRows = 32;   // rows a warp resolves at once (a lane per row)
+constexpr int kSendMaxSrc = 8;  // sources per row kept from that resolution
 
-// Warp per received row (r, s), found like permute_received_kernel's rows (prefix of
-// the per-rank counts in shared memory, binary search). Lanes j < k resolve the row's
-// local experts to their expert-major rows, compacted in slot order by a ballot; then the
-// warp walks the row kSendGroups x 32 vectors at a time with up to kSendBatch x
-// kSendGroups source vectors in flight per lane, adding strictly in slot order (one fp32
-// multiply by the row's weight and one fp32 add per term, never fused), and stores one
-// bf16 vector per group, rounded to nearest even. A row with a single local expert (most
-// rows) keeps kSendWide groups of loads in flight and computes 0 + term per channel.
-__global__ void __launch_bounds__(kThreads) combine_send_kernel(CombineSendArgs a) {
+// Copies one rank-level row from its ns compacted sources (expert-major row offsets in
+// units of 16-byte vectors, weights), strictly in slot order: acc = 0, then per term one
+// fp32 multiply by the weight (when weighted) and one fp32 add, never fused; one rounding
+// to bf16 at the end.
+__device__ __forceinline__ void send_row(const CombineSendArgs& a, const uint4* ys, uint4* dst, int nvec, int ns,
+                                         const long long* srcs, const float* ws) {
+    const int lane = lane_id();
+    if (ns == 1) {
+        // one local expert (most rows): acc = 0 + term, kSendWide groups of loads in flight
+        const uint4* src1 = ys + srcs[0];
+        const float w = ws[0];
+        for (int v0 = lane; v0 < nvec; v0 += 32 * kSendWide) {
+            uint4 buf[kSendWide];
+#pragma unroll
+            for (int g = 0; g < kSendWide; ++g)
+                if (v0 + 32 * g < nvec) buf[g] = ld_stream_v4(src1 + v0 + 32 * g);
+#pragma unroll
+            for (int g = 0; g < kSendWide; ++g) {
+                if (v0 + 32 * g >= nvec) continue;
+                const uint32_t wd[4] = {buf[g].x, buf[g].y, buf[g].z, buf[g].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float lo = a.recv_tw != nullptr ? __fmul_rn(bf16_lo(wd[h]), w) : bf16_lo(wd[h]);
+                    const float hi = a.recv_tw != nullptr ? __fmul_rn(bf16_hi(wd[h]), w) : bf16_hi(wd[h]);
+                    o[h] = pack_bf16x2_rn(__fadd_rn(0.0f, lo), __fadd_rn(0.0f, hi));
+                }
+                st_v4(dst + v0 + 32 * g, make_uint4(o[0], o[1], o[2], o[3]));
+            }
+        }
+        return;
+    }
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kSendGroups) {
+        float acc[kSendGroups][8];
+#pragma unroll
+        for (int g = 0; g < kSendGroups; ++g)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[g][i] = 0.0f;
+        for (int d0 = 0; d0 < ns; d0 += kSendBatch) {
+            uint4 buf[kSendBatch][kSendGroups];
+#pragma unroll
+            for (int b = 0; b < kSendBatch; ++b)
+#pragma unroll
+                for (int g = 0; g < kSendGroups; ++g)
+                    if (d0 + b < ns && v0 + 32 * g < nvec) buf[b][g] = ld_stream_v4(ys + srcs[d0 + b] + v0 + 32 * g);
+#pragma unroll
+            for (int b = 0; b < kSendBatch; ++b) {
+                if (d0 + b >= ns) continue;
+                const float w = ws[d0 + b];
+#pragma unroll
+                for (int g = 0; g < kSendGroups; ++g) {
+                    const uint32_t wd[4] = {buf[b][g].x, buf[b][g].y, buf[b][g].z, buf[b][g].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        if (a.recv_tw != nullptr) {
+                            acc[g][2 * h] = __fadd_rn(acc[g][2 * h], __fmul_rn(bf16_lo(wd[h]), w));
+                            acc[g][2 * h + 1] = __fadd_rn(acc[g][2 * h + 1], __fmul_rn(bf16_hi(wd[h]), w));
+                        } else {
+                            acc[g][2 * h] = __fadd_rn(acc[g][2 * h], bf16_lo(wd[h]));
+                            acc[g][2 * h + 1] = __fadd_rn(acc[g][2 * h + 1], bf16_hi(wd[h]));
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < kSendGroups; ++g) {
+            if (v0 + 32 * g < nvec) {
+                uint4 o;
+                o.x = pack_bf16x2_rn(acc[g][0], acc[g][1]);
+                o.y = pack_bf16x2_rn(acc[g][2], acc[g][3]);
+                o.z = pack_bf16x2_rn(acc[g][4], acc[g][5]);
+                o.w = pack_bf16x2_rn(acc[g][6], acc[g][7]);
+                st_v4(dst + v0 + 32 * g, o);
+            }
+        }
+    }
+}
+
+// Each warp owns a contiguous share of the received rows and takes it kSendRows rows at a
+// time. Phase 1, a lane per row: the row (r, s) is
+// found from the prefix of the per-rank counts in shared memory (binary search), and its
+// local experts are resolved to expert-major rows -- received id, expert slot, offsets --
+// so the dependent metadata loads of 32 rows overlap instead of running row after row.
+// Up to kSendMaxSrc sources per row are kept in shared memory, in slot order; a row with
+// more local experts is resolved again by the whole warp (lanes across slots) when its turn
+// comes. Phase 2 copies the batch's rows one after another (send_row).
+__global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendArgs a) {
     grid_dependency_wait();  // dependent launch: the expert outputs are complete after this
+    __shared__ long long s_bsrc[kWarps][kSendRows][kSendMaxSrc];
+    __shared__ float s_bw[kWarps][kSendRows][kSendMaxSrc];
+    __shared__ int s_bns[kWarps][kSendRows];
+    __shared__ long long s_brow[kWarps][kSendRows];
+    __shared__ int s_bt[kWarps][kSendRows];
     __shared__ long long s_src[kWarps][kMaxTopk];
     __shared__ float s_w[kWarps][kMaxTopk];
     __shared__ int s_base[257];
@@ -773,115 +859,98 @@ __global__ void __launch_bounds__(kThreads) combine_send_kernel(CombineSendArgs 
     const int total = s_base[a.R];
     const uint4* ys = reinterpret_cast<const uint4*>(a.y_perm);
     uint4* outs = reinterpret_cast<uint4*>(a.y_rank);
-    for (int q = blockIdx.x * kWarps + warp; q < total; q += gridDim.x * kWarps) {
-        int lo = 0, hi = a.R;  // last r with s_base[r] <= q
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (s_base[mid] <= q) lo = mid;
-            else hi = mid;
-        }
-        const int r = lo;
-        const size_t row = static_cast<size_t>(r) * a.max_tokens + (q - s_base[r]);
-        const int t = a.recv_src[row];
-        bool ok = false, over = false;
-        long long src = 0;
-        float wj = 1.0f;
-        if (lane < a.k && t >= 0 && t < a.T) {
-            const int l = a.recv_tidx[row * a.k + lane];
-            const int32_t sl = a.eslot[static_cast<size_t>(t) * a.k + lane];
-            if (l >= 0 && l < epr && sl >= 0) {
-                const int p = a.offsets[r * epr + l] - a.offsets[r * epr] + sl;
-                if (p >= 0 && p < a.max_rows) {
-                    ok = true;
-                    src = (static_cast<long long>(r) * a.max_rows + p) * nvec;
-                    if (a.recv_tw != nullptr) wj = a.recv_tw[row * a.k + lane];
-                } else {
-                    over = true;
+    // each warp owns a contiguous share of the rows, resolved up to kSendRows at a time
+    const int nwarps = static_cast<int>(gridDim.x) * kWarps;
+    const int share = (total + nwarps - 1) / nwarps;
+    const int q_begin = (static_cast<int>(blockIdx.x) * kWarps + warp) * share;
+    const int q_end = q_begin + share < total ? q_begin + share : total;
+    for (int q0 = q_begin; q0 < q_end; q0 += kSendRows) {
+        const int nb = q_end - q0 < kSendRows ? q_end - q0 : kSendRows;
+        // phase 1: lane i resolves row q0 + i
+        const int q = q0 + lane;
+        int n = 0, t = -1;
+        bool over = false;
+        long long orow = 0;
+        if (lane < nb) {
+            int lo = 0, hi = a.R;  // last r with s_base[r] <= q
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_base[mid] <= q) lo = mid;
+                else hi = mid;
+            }
+            const int r = lo;
+            orow = static_cast<long long>(r) * a.max_tokens + (q - s_base[r]);
+            t = a.recv_src[orow];
+            if (t >= 0 && t < a.T) {
+                const int base = a.offsets[r * epr];
+                for (int j0 = 0; j0 < a.k; j0 += 8) {
+                    int lv[8], sv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        lv[i] = j0 + i < a.k ? a.recv_tidx[orow * a.k + j0 + i] : -1;
+                        sv[i] = j0 + i < a.k ? a.eslot[static_cast<size_t>(t) * a.k + j0 + i] : -1;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (lv[i] < 0 || lv[i] >= epr || sv[i] < 0) continue;
+                        const int p = a.offsets[r * epr + lv[i]] - base + sv[i];
+                        if (p < 0 || p >= a.max_rows) {
+                            over = true;
+                            continue;
+                        }
+                        if (n < kSendMaxSrc) {
+                            s_bsrc[warp][lane][n] = (static_cast<long long>(r) * a.max_rows + p) * nvec;
+                            s_bw[warp][lane][n] = a.recv_tw != nullptr ? a.recv_tw[orow * a.k + j0 + i] : 1.0f;
+                        }
+                        ++n;
+                    }
                 }
             }
         }
-        const uint32_t m = __ballot_sync(kFullMask, ok);
-        if (ok) {
-            const int pos = __popc(m & lanemask_lt());
-            s_src[warp][pos] = src;
-            s_w[warp][pos] = wj;
-        }
+        s_bns[warp][lane] = n;
+        s_brow[warp][lane] = orow;
+        s_bt[warp][lane] = t;
         if (__any_sync(kFullMask, over) && lane == 0) raise_flag(a.status, EP_FLAG_CAPACITY);
         __syncwarp();
-        const int ns = __popc(m);
-        uint4* dst = outs + row * nvec;
-        if (ns == 1) {
-            // one local expert (most rows): acc = 0 + term, kSendWide groups of loads in flight
-            const uint4* src1 = ys + s_src[warp][0];
-            const float w = s_w[warp][0];
-            for (int v0 = lane; v0 < nvec; v0 += 32 * kSendWide) {
-                uint4 buf[kSendWide];
-#pragma unroll
-                for (int g = 0; g < kSendWide; ++g)
-                    if (v0 + 32 * g < nvec) buf[g] = ld_stream_v4(src1 + v0 + 32 * g);
-#pragma unroll
-                for (int g = 0; g < kSendWide; ++g) {
-                    if (v0 + 32 * g >= nvec) continue;
-                    const uint32_t wd[4] = {buf[g].x, buf[g].y, buf[g].z, buf[g].w};
-                    uint32_t o[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float lo = a.recv_tw != nullptr ? __fmul_rn(bf16_lo(wd[h]), w) : bf16_lo(wd[h]);
-                        const float hi = a.recv_tw != nullptr ? __fmul_rn(bf16_hi(wd[h]), w) : bf16_hi(wd[h]);
-                        o[h] = pack_bf16x2_rn(__fadd_rn(0.0f, lo), __fadd_rn(0.0f, hi));
-                    }
-                    st_v4(dst + v0 + 32 * g, make_uint4(o[0], o[1], o[2], o[3]));
-                }
-            }
-            __syncwarp();
-            continue;
-        }
-        for (int v0 = lane; v0 < nvec; v0 += 32 * kSendGroups) {
-            float acc[kSendGroups][8];
-#pragma unroll
-            for (int g = 0; g < kSendGroups; ++g)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[g][i] = 0.0f;
-            for (int d0 = 0; d0 < ns; d0 += kSendBatch) {
-                uint4 buf[kSendBatch][kSendGroups];
-#pragma unroll
-                for (int b = 0; b < kSendBatch; ++b)
-#pragma unroll
-                    for (int g = 0; g < kSendGroups; ++g)
-                        if (d0 + b < ns && v0 + 32 * g < nvec) buf[b][g] = ld_stream_v4(ys + s_src[warp][d0 + b] + v0 + 32 * g);
-#pragma unroll
-                for (int b = 0; b < kSendBatch; ++b) {
-                    if (d0 + b >= ns) continue;
-                    const float w = s_w[warp][d0 + b];
-#pragma unroll
-                    for (int g = 0; g < kSendGroups; ++g) {
-                        const uint32_t wd[4] = {buf[b][g].x, buf[b][g].y, buf[b][g].z, buf[b][g].w};
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            if (a.recv_tw != nullptr) {
-                                acc[g][2 * h] = __fadd_rn(acc[g][2 * h], __fmul_rn(bf16_lo(wd[h]), w));
-                                acc[g][2 * h + 1] = __fadd_rn(acc[g][2 * h + 1], __fmul_rn(bf16_hi(wd[h]), w));
-                            } else {
-                                acc[g][2 * h] = __fadd_rn(acc[g][2 * h], bf16_lo(wd[h]));
-                                acc[g][2 * h + 1] = __fadd_rn(acc[g][2 * h + 1], bf16_hi(wd[h]));
-                            }
+        // phase 2: the batch's rows
+        for (int i = 0; i < nb; ++i) {
+            int ns = s_bns[warp][i];
+            const long long row = s_brow[warp][i];
+            const long long* srcs = s_bsrc[warp][i];
+            const float* ws = s_bw[warp][i];
+            if (ns > kSendMaxSrc) {
+                // more local experts than phase 1 kept: lanes across slots, compacted by a ballot
+                const int r = static_cast<int>(row / a.max_tokens);
+                const int tt = s_bt[warp][i];
+                bool ok = false;
+                long long src = 0;
+                float wj = 1.0f;
+                if (lane < a.k) {
+                    const int l = a.recv_tidx[row * a.k + lane];
+                    const int32_t sl = a.eslot[static_cast<size_t>(tt) * a.k + lane];
+                    if (l >= 0 && l < epr && sl >= 0) {
+                        const int p = a.offsets[r * epr + l] - a.offsets[r * epr] + sl;
+                        if (p >= 0 && p < a.max_rows) {
+                            ok = true;
+                            src = (static_cast<long long>(r) * a.max_rows + p) * nvec;
+                            if (a.recv_tw != nullptr) wj = a.recv_tw[row * a.k + lane];
                         }
                     }
                 }
-            }
-#pragma unroll
-            for (int g = 0; g < kSendGroups; ++g) {
-                if (v0 + 32 * g < nvec) {
-                    uint4 o;
-                    o.x = pack_bf16x2_rn(acc[g][0], acc[g][1]);
-                    o.y = pack_bf16x2_rn(acc[g][2], acc[g][3]);
-                    o.z = pack_bf16x2_rn(acc[g][4], acc[g][5]);
-                    o.w = pack_bf16x2_rn(acc[g][6], acc[g][7]);
-                    st_v4(dst + v0 + 32 * g, o);
+                const uint32_t m = __ballot_sync(kFullMask, ok);
+                if (ok) {
+                    const int pos = __popc(m & lanemask_lt());
+                    s_src[warp][pos] = src;
+                    s_w[warp][pos] = wj;
                 }
+                __syncwarp();
+                ns = __popc(m);
+                srcs = s_src[warp];
+                ws = s_w[warp];
             }
+            send_row(a, ys, outs + row * nvec, nvec, ns, srcs, ws);
+            __syncwarp();
         }
-        __syncwarp();
     }
     allow_dependents();
 }

@@ -872,6 +872,83 @@ def extra_stages(ep, dev, args, flush, peak):
     return res
 
 
+# --------------------------------------------------------------------------- profiling runs
+
+PROFILE_STAGES = ("step", "sustained", "restripe", "send", "fp8")
+
+
+def profile_stage(name):
+    """Run one stage's kernels three times, L2 flushed before each, and exit: a small, fixed
+    program for ncu captures (no timing, no JSON line). step: the dsv3 layout, dispatch and
+    combine; sustained: the dsv3 step on 8 distinct buffer sets back to back; restripe: the
+    prob restripe (T=8192, 8 nodes, P=128); send: the dsv3 send phase of the split combine;
+    fp8: the dsv3 FP8 dispatch, then the FP8-input combine of its rows."""
+    import combine_ep_get_05_gb300 as ep
+
+    ep.build_library()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    flush = L2Flush(dev)
+
+    def load(wname, **over):
+        w = workloads.make(wname, **over)
+        x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+        return w, x, torch.from_numpy(w.topk_idx).to(dev), torch.from_numpy(w.topk_w).to(dev)
+
+    if name in ("step", "sustained"):
+        w, x, topk, tw = load("dsv3")
+        M = w.max_tokens
+        sets = [(x.clone(), topk.clone(), tw.clone(), ep.alloc_layout(w.T, w.E, w.R, w.ranks_per_node, dev),
+                 ep.alloc_dispatch(w.R, M, w.H, w.k, device=dev), torch.empty((w.T, w.H), dtype=torch.bfloat16,
+                                                                              device=dev))
+                for _ in range(8 if name == "sustained" else 1)]
+        for _ in range(3):
+            flush()
+            for xx, tk, ww, lay, d, out in sets:
+                ep.get_layout(tk, w.E, w.R, w.ranks_per_node, out=lay)
+                ep.dispatch(xx, tk, ww, lay, M, out=d)
+                ep.combine(d.recv_x, lay, M, out=out)
+    elif name == "restripe":
+        w = workloads.make("restripe")
+        prob = torch.from_numpy(w.prob).to(dev)
+        out = torch.empty((w.num_nodes, w.max_tokens, w.prob.shape[2]), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            flush()
+            ep.ep_restripe_prob(prob, w.max_tokens, out)
+    elif name == "send":
+        w, x, topk, tw = load("dsv3")
+        E, R, T, H, k = w.E, w.R, w.T, w.H, w.k
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        eslot = torch.empty((T, k), dtype=torch.int32, device=dev)
+        ews = torch.zeros(ep.ep_expert_layout_workspace_size(T, E), dtype=torch.uint8, device=dev)
+        ep.ep_get_expert_layout(topk, E, off, eslot, ews)
+        offs = off.cpu().numpy()
+        Mp = int(max(offs[(r + 1) * (E // R)] - offs[r * (E // R)] for r in range(R)))
+        px = torch.empty((R, Mp, H), dtype=torch.bfloat16, device=dev)
+        ep.ep_dispatch_permuted(x, topk, tw, off, eslot, E, R, Mp, px)
+        lay = ep.get_layout(topk, E, R, w.ranks_per_node)
+        d = ep.dispatch(x, topk, tw, lay, w.max_tokens)
+        yr = torch.empty((R, w.max_tokens, H), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            flush()
+            ep.ep_combine_send(px, d.recv_src_idx, d.recv_topk_idx, d.recv_topk_w, lay.tokens_per_rank, off, eslot,
+                               E, yr)
+    elif name == "fp8":
+        w, x, topk, tw = load("dsv3_fp8")
+        lay = ep.get_layout(topk, w.E, w.R, w.ranks_per_node)
+        d = ep.alloc_dispatch(w.R, w.max_tokens, w.H, w.k, fp8=True, device=dev)
+        out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            flush()
+            ep.dispatch(x, topk, tw, lay, w.max_tokens, fp8=True, out=d)
+            flush()
+            ep.combine_fp8(d.recv_x, d.recv_scales, lay, w.max_tokens, out=out)
+    else:
+        raise ValueError(f"unknown stage {name!r}; expected one of {PROFILE_STAGES}")
+    torch.cuda.synchronize()
+    log(f"profile stage {name}: done")
+
+
 # --------------------------------------------------------------------------- reference arm
 
 def run_reference(args, world, rank):
@@ -916,7 +993,12 @@ def main(argv=None):
     ap.add_argument("--skip-extra", action="store_true", help="skip the other workloads' stage timings")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer measurement")
     ap.add_argument("--soak-s", type=float, default=1.0, help="untimed load before the timed steps (clocks)")
+    ap.add_argument("--profile", choices=PROFILE_STAGES, default=None,
+                    help="run one stage's kernels three times for a profiler capture, then exit (no timing)")
     args = ap.parse_args(argv)
+    if args.profile is not None:
+        profile_stage(args.profile)
+        return 0
     if args.warmup < 3:
         log("warmup raised to 3 (minimum)")
         args.warmup = 3

@@ -268,7 +268,9 @@ def host_cpu():
             imp = [line.split(":")[1].strip() for line in info.splitlines() if line.startswith("CPU implementer")]
             part = [line.split(":")[1].strip() for line in info.splitlines() if line.startswith("CPU part")]
             if imp and part:
-                model = f"Arm implementer {imp[0]} part {part[0]}"
+                known = {("0x41", "0xd4f"): "Arm Neoverse V2", ("0x41", "0xd40"): "Arm Neoverse V1",
+                         ("0x41", "0xd0c"): "Arm Neoverse N1", ("0x41", "0xd49"): "Arm Neoverse N2"}
+                model = known.get((imp[0].lower(), part[0].lower()), f"Arm implementer {imp[0]} part {part[0]}")
     except OSError:
         pass
     import platform

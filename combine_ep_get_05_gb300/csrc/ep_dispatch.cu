@@ -17,6 +17,8 @@
 // (source index, local expert ids, weights) is written by one lane per
 // destination. Nothing here is a contraction, so no tensor cores: the kernel
 // is bound by HBM bandwidth (read T rows, write one row per (token, rank)).
+#include <algorithm>
+
 #include "ep_common.cuh"
 #include "ep_scatter.cuh"
 
@@ -29,6 +31,7 @@ constexpr int kMaxTopk = 32;
 constexpr int kUnroll = 8;     // 16-byte vectors in flight per lane (bf16 path)
 constexpr int kRegDest = 8;    // destinations whose row offsets a warp keeps in registers
 constexpr int kUnrollFp8 = 2;  // warp iterations (4 blocks of 128 each) in flight (FP8 path)
+constexpr uint32_t kFp8BulkMaxSmem = 52 * 1024;  // shared memory of the bulk FP8 kernel (4 CTAs per SM)
 
 struct DispatchArgs {
     const uint16_t* x;
@@ -311,6 +314,193 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a, 
     }
 }
 
+// FP8 dispatch through shared memory and bulk copies: a CTA of 8 warps takes one token at a
+// time (tokens blockIdx.x, +gridDim.x, ...). Thread 0 streams the tokens' bf16 rows into two
+// shared-memory row buffers with bulk global->shared copies (two tokens ahead, completing on
+// mbarriers); for each token the 8 warps quantise the row from shared memory -- 8 lanes per
+// 128-element block, the quantiser of the register kernel -- into a staging code row (H
+// bytes) and scale row (H/128 floats) in shared memory; thread 0 sends the code row to every
+// destination with one bulk shared->global copy, and warp 0 writes the small scale rows with
+// 16-byte stores. The staging rows are double-buffered:
+// a token writes the buffer its predecessor's predecessor used once those stores have read
+// it, so the stores of one token overlap the quantisation of the next. No code passes
+// through a store from registers; the SM's work per byte is the quantiser's. Warp 0 resolves
+// each token's destinations and writes its metadata, from the slot row, ids and weights it
+// loaded into registers while the previous token was quantised. Every barrier wait is bounded; on
+// timeout the CTA waits (bounded) for its loads in flight, raises EP_FLAG_TIMEOUT and stops.
+// Used when H % 512 == 0 (scale rows of whole 16-byte vectors) and the buffers fit.
+struct Fp8Smem {
+    uint32_t row_bytes, code_bytes, scale_bytes;
+    uint32_t row_stride;    // row buffer b at b * row_stride
+    uint32_t stage_base;    // staging buffer b at stage_base + b * stage_stride: codes, then scales
+    uint32_t stage_stride;
+    uint32_t scale_off;     // scales within a staging buffer
+    uint32_t total;
+};
+
+inline Fp8Smem fp8_smem_layout(int H) {
+    auto up = [](uint32_t n) { return (n + 127u) & ~127u; };
+    Fp8Smem m{};
+    m.row_bytes = static_cast<uint32_t>(H) * 2u;
+    m.code_bytes = static_cast<uint32_t>(H);
+    m.scale_bytes = static_cast<uint32_t>(H / 128) * 4u;
+    m.row_stride = up(m.row_bytes);
+    m.stage_base = 2u * m.row_stride;
+    m.scale_off = up(m.code_bytes);
+    m.stage_stride = m.scale_off + up(m.scale_bytes);
+    m.total = m.stage_base + 2u * m.stage_stride;
+    return m;
+}
+
+__global__ void __launch_bounds__(kThreads, 4) dispatch_fp8_bulk_kernel(DispatchArgs a, Fp8Smem m) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t s_bar[2];
+    __shared__ int s_rank[kMaxDest];
+    __shared__ long long s_row[kMaxDest];
+    __shared__ int s_nd, s_ok;
+    ep::grid_dependency_wait();  // dependent launch: inputs are ready after this
+    const int tid = static_cast<int>(threadIdx.x);
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nblk = a.H / 128;
+    const int grp = lane >> 3;
+    const int pos = lane & 7;
+    const int first = static_cast<int>(blockIdx.x);
+    const int step = static_cast<int>(gridDim.x);
+    const int n_my = first < a.T ? (a.T - 1 - first) / step + 1 : 0;
+    uint8_t* recv = static_cast<uint8_t*>(a.recv_x);
+    int issued = 0;  // row loads issued by thread 0
+    if (tid == 0) {
+        ep::mbar_init(&s_bar[0], 1);
+        ep::mbar_init(&s_bar[1], 1);
+        ep::mbar_init_fence();
+        for (; issued < 2 && issued < n_my; ++issued) {
+            ep::mbar_arrive_expect_tx(&s_bar[issued], m.row_bytes);
+            ep::bulk_load(smem + issued * m.row_stride, a.x + static_cast<size_t>(first + issued * step) * a.H,
+                          m.row_bytes, &s_bar[issued]);
+        }
+        s_ok = 1;
+    }
+    __syncthreads();
+    // warp 0 holds the next token's slot row (lane r + 32c), top-k ids and weights (lane j)
+    // in registers, loaded a token ahead so that their latency hides behind a quantisation
+    int sv[kMaxDest / 32];
+    long long idv = -1;
+    float wv = 0.0f;
+    auto fetch_meta = [&](int t) {
+#pragma unroll
+        for (int c = 0; c < kMaxDest / 32; ++c) {
+            const int r = c * 32 + lane;
+            sv[c] = (c * 32 < a.R && r < a.R) ? a.slot[static_cast<size_t>(t) * a.R + r] : -1;
+        }
+        idv = lane < a.k ? a.topk_idx[static_cast<size_t>(t) * a.k + lane] : -1;
+        wv = (lane < a.k && a.recv_topk_w != nullptr) ? a.topk_w[static_cast<size_t>(t) * a.k + lane] : 0.0f;
+    };
+    if (warp == 0 && n_my > 0) fetch_meta(first);
+    int i = 0;
+    for (; i < n_my; ++i) {
+        const int t = first + i * step;
+        const int b = i & 1;
+        if (warp == 0) {
+            // destinations of token t (ascending rank; slots >= max_tokens dropped)
+            int nd = 0;
+            bool over_any = false;
+#pragma unroll
+            for (int c = 0; c < kMaxDest / 32; ++c) {
+                if (c * 32 >= a.R) break;
+                const int r = c * 32 + lane;
+                const int sl = sv[c];
+                const bool over = sl >= a.max_tokens;
+                over_any |= over;
+                const bool ok = r < a.R && sl >= 0 && !over;
+                const uint32_t msk = __ballot_sync(ep::kFullMask, ok);
+                if (ok) {
+                    const int p = nd + __popc(msk & ep::lanemask_lt());
+                    s_rank[p] = r;
+                    s_row[p] = static_cast<long long>(r) * a.max_tokens + sl;
+                }
+                nd += __popc(msk);
+            }
+            if (__any_sync(ep::kFullMask, over_any) && lane == 0) ep::raise_flag(a.status, EP_FLAG_CAPACITY);
+            if (__any_sync(ep::kFullMask, idv >= a.E) && lane == 0) ep::raise_flag(a.status, EP_FLAG_BAD_EXPERT);
+            __syncwarp();
+            // metadata: lane j writes slot j of every destination's rows
+            for (int d = 0; d < nd; ++d) {
+                const int r = s_rank[d];
+                const size_t row = static_cast<size_t>(s_row[d]);
+                if (lane == 0 && a.recv_src_idx != nullptr) a.recv_src_idx[row] = t;
+                if (lane < a.k) {
+                    const bool on = idv >= 0 && idv < a.E && static_cast<int>(idv) / a.epr == r;
+                    if (a.recv_topk_idx != nullptr)
+                        a.recv_topk_idx[row * a.k + lane] = on ? static_cast<int32_t>(idv) - r * a.epr : -1;
+                    if (a.recv_topk_w != nullptr) a.recv_topk_w[row * a.k + lane] = on ? wv : 0.0f;
+                }
+            }
+            if (i + 1 < n_my) fetch_meta(t + step);
+            if (lane == 0) {
+                s_nd = nd;
+                // staging buffer b was read by the stores of token i - 2: all but the newest
+                // bulk group (token i - 1) must have finished reading
+                ep::bulk_wait_read<1>();
+                if (!ep::mbar_wait_bounded(&s_bar[b], static_cast<uint32_t>((i >> 1) & 1))) s_ok = 0;
+            }
+        }
+        __syncthreads();
+        if (!s_ok) break;
+        const int nd = s_nd;
+        const uint16_t* row = reinterpret_cast<const uint16_t*>(smem + b * m.row_stride);
+        uint8_t* codes = smem + m.stage_base + b * m.stage_stride;
+        float* scales = reinterpret_cast<float*>(codes + m.scale_off);
+        if (nd > 0) {
+            // thread 0 saw the row's barrier complete; every reader observes that phase too
+            (void)ep::mbar_wait_bounded(&s_bar[b], static_cast<uint32_t>((i >> 1) & 1));
+            // a warp's 4 blocks are all in range or all out of it (nblk % 4 == 0), so the
+            // quantiser's shuffles always run on whole warps
+            for (int blk = warp * 4 + grp; blk < nblk; blk += kWarps * 4) {
+                const uint4* src = reinterpret_cast<const uint4*>(row + blk * 128 + pos * 16);
+                uint4 q;
+                float sc;
+                quantize16(src[0], src[1], q, sc);
+                *reinterpret_cast<uint4*>(codes + blk * 128 + pos * 16) = q;
+                if (pos == 0) scales[blk] = sc;
+            }
+            ep::fence_proxy_async_smem();
+        }
+        __syncthreads();
+        if (warp == 0) {  // warp 0 also rewrites the destination list next token: program order
+            if (lane == 0) {
+                for (int d = 0; d < nd; ++d)
+                    ep::bulk_store(recv + static_cast<size_t>(s_row[d]) * a.H, codes, m.code_bytes);
+                ep::bulk_commit();
+                // row buffer b is free (every warp has quantised token i): token i + 2 goes there
+                if (issued < n_my) {
+                    ep::mbar_arrive_expect_tx(&s_bar[b], m.row_bytes);
+                    ep::bulk_load(smem + b * m.row_stride, a.x + static_cast<size_t>(first + issued * step) * a.H,
+                                  m.row_bytes, &s_bar[b]);
+                    ++issued;
+                }
+            }
+            // the scale rows: 16 bytes per lane, one store instruction per destination
+            for (int d = 0; d < nd; ++d) {
+                float* dsc = a.recv_scales + static_cast<size_t>(s_row[d]) * nblk;
+                for (int v = lane; v < nblk / 4; v += 32)
+                    ep::st_v4(dsc + 4 * v, *reinterpret_cast<const uint4*>(scales + 4 * v));
+            }
+        }
+    }
+    ep::allow_dependents();
+    if (tid == 0) {
+        if (!s_ok) {
+            for (int q = i; q < issued; ++q)  // row i timed out: wait (bounded) for every load in flight
+                (void)ep::mbar_wait_bounded(&s_bar[q & 1], static_cast<uint32_t>((q >> 1) & 1));
+            ep::raise_flag(a.status, EP_FLAG_TIMEOUT);
+        }
+        ep::bulk_wait_all();
+    }
+}
+
+std::atomic<int> g_fp8_bulk_smem_set[ep::kMaxDevices];
+
 std::atomic<int> g_fp8_per_sm[ep::kMaxDevices];
 
 int grid_for(int T, int blocks_per_sm) {
@@ -361,6 +551,15 @@ extern "C" ep_status_t ep_dispatch(const void* x, ep_dtype_t out_dtype, const in
     a.recv_topk_w = recv_topk_w;
     a.status = status;
     if (fp8) {
+        const Fp8Smem m = fp8_smem_layout(H);
+        if (H % 512 == 0 && m.total <= kFp8BulkMaxSmem) {
+            const ep_status_t attr =
+                ensure_dynamic_smem(g_fp8_bulk_smem_set, dispatch_fp8_bulk_kernel, static_cast<int>(kFp8BulkMaxSmem));
+            if (attr != EP_OK) return attr;
+            const long long grid = std::min<long long>(T, static_cast<long long>(sm_count()) * 4);
+            return launch_dependent(dispatch_fp8_bulk_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                                    static_cast<size_t>(m.total), as_stream(stream), a, m);
+        }
         int per_sm = 1;
         const ep_status_t occ = blocks_per_sm(g_fp8_per_sm, dispatch_fp8_kernel, kThreads, 0, &per_sm);
         if (occ != EP_OK) return occ;

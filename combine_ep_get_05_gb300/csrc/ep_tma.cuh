@@ -46,12 +46,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap& map, int x, int 
                  : "memory");
 }
 
-// all committed bulk stores of this thread but the newest `N` have finished reading shared memory
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap& m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap_addr(m)) : "memory");
 }

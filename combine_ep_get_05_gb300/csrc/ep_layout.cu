@@ -424,13 +424,12 @@ std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of g_layout_scratch on the current device (host code must not use the
-// symbol itself: on the host it names a host-side shadow, not device memory). Outside
-// stream capture the address is looked up on every call (cudaGetSymbolAddress is a cheap
-// host call) and remembered, so a context created anew (after cudaDeviceReset) is picked
-// up at once. While `stream` is being captured the remembered address is used instead,
-// because the lookup may have to load the module, which a capture must not see; if no
-// call outside capture has been made on this device yet, the call is refused
-// (EP_ERR_INVALID) before anything is recorded into the graph.
+// symbol itself: on the host it names a host-side shadow, not device memory). The address
+// is looked up on every call (cudaGetSymbolAddress is a cheap host call) and remembered,
+// so a context created anew (after cudaDeviceReset) is picked up at once. A call made
+// while `stream` is capturing does not look it up (the lookup may have to load the
+// module) and uses the remembered address; with none remembered it is refused
+// (EP_ERR_INVALID) before anything is queued.
 ep_status_t scratch_address(cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);

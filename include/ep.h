@@ -138,13 +138,10 @@ ep_status_t ep_get_layout(const int64_t* topk_idx, int32_t T, int32_t k, int32_t
  * fixed-size array inside the library (EP_LAYOUT_NOALLOC_SCRATCH_BYTES of
  * device memory that every GPU which loads the library keeps until the process
  * exits). It never calls cudaMalloc, cudaFree or any allocating routine.
- *   - Outside stream capture, every call looks up that array's device address
- *     (cudaGetSymbolAddress, with the device current) and remembers it per
- *     device. While `stream` is being captured into a CUDA graph the remembered
- *     address is used: a captured call made before any uncaptured call on that
- *     device returns EP_ERR_INVALID and records nothing, so make one call
- *     outside capture first (and again after cudaDeviceReset, which gives the
- *     array a new address).
+ *   - Each call looks up that array's device address (cudaGetSymbolAddress,
+ *     with the device current) and remembers it per device; a call made while
+ *     `stream` is capturing uses the remembered address instead, and returns
+ *     EP_ERR_INVALID (nothing queued) when none has been remembered yet.
  *   - Each call zero-fills the part of the array it uses (an async memset on
  *     `stream`), then launches the layout kernel.
  *   - Sizes whose workspace (ep_layout_workspace_size) exceeds

@@ -48,6 +48,7 @@ FLUSH_BYTES = 256 << 20
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_HBM_GBS = 6800.0
+STAGE_ITERATIONS = 50  # timed replays per extra stage (median, p10 and p90 reported)
 
 
 def log(*a):
@@ -510,6 +511,9 @@ def run_ours(args, world, rank):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "ms_per_step_median": round(statistics.median(step_ms), 4),
+        "ms_per_step_p10": round(float(np.percentile(step_ms, 10)), 4),
+        "ms_per_step_p90": round(float(np.percentile(step_ms, 90)), 4),
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "dsv3 prefill: T=4096 H=7168 bf16, E=256 top-8, R=32 virtual ranks "
                                "(8 nodes x 4), max_tokens=4096, identity expert",
@@ -632,19 +636,34 @@ def sustained_step(ep, dev, args, flush, peak, K=8):
             ep.dispatch(st["x"], st["topk"], st["tw"], st["lay"], M, out=st["d"])
             ep.combine(st["d"].recv_x, st["lay"], M, out=st["out"])
 
-    ms = time_events(run, max(3, min(args.steps, 10)), flush, stream) / K
+    times = time_events(run, max(3, min(args.steps, 10)), flush, stream)
+    ms = float(times) / K
     pairs = int(sets[0]["lay"].tokens_per_rank.sum().item())
     assert torch.equal(sets[-1]["out"], sets[0]["out"])
     total = sum(step_bytes(T, H, k, E, R, w.num_nodes, pairs).values())
     del sets
-    return {"steps_per_replay": K, "ms_per_step": round(ms, 4), "alg_bytes_per_step": total,
+    return {"steps_per_replay": K, "ms_per_step": round(ms, 4), "ms_per_step_p10": round(times.p10 / K, 4),
+            "ms_per_step_p90": round(times.p90 / K, 4), "replays": times.n, "alg_bytes_per_step": total,
             "gbs": round(total / (ms * 1e-3) / 1e9, 1), "frac_of_hbm_peak": round(total / (ms * 1e-3) / 1e9 / peak, 4),
             "tokens_per_s": round(T / (ms * 1e-3), 1),
             "timing": f"{K} steps on {K} distinct buffer sets in one graph; L2 flushed before each replay only"}
 
 
+class Times(float):
+    """Mean device time (ms) of timed replays, carrying their median, 10th and 90th
+    percentiles and count."""
+
+    def __new__(cls, samples):
+        obj = float.__new__(cls, statistics.mean(samples))
+        obj.median = statistics.median(samples)
+        obj.p10 = float(np.percentile(samples, 10))
+        obj.p90 = float(np.percentile(samples, 90))
+        obj.n = len(samples)
+        return obj
+
+
 def time_events(fn, n, flush, stream):
-    """Mean device time of fn, captured in a CUDA graph, L2 flushed before each replay."""
+    """Device time of fn, captured in a CUDA graph, L2 flushed before each of n replays."""
     g = capture(fn)
     ms = []
     for _ in range(n):
@@ -655,7 +674,7 @@ def time_events(fn, n, flush, stream):
         z.record(stream)
         ms.append((a, z))
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(z) for a, z in ms)
+    return Times([a.elapsed_time(z) for a, z in ms])
 
 
 def extra_stages(ep, dev, args, flush, peak):
@@ -663,12 +682,19 @@ def extra_stages(ep, dev, args, flush, peak):
     restripe + node dispatch,
     skewed routing). Each is timed with CUDA events, L2 flushed before every launch."""
     stream = torch.cuda.current_stream()
-    n = max(3, min(args.steps, 10))
-    res = {}
+    n = STAGE_ITERATIONS
+    res = {"iterations_per_stage": n}
 
-    def gbs(bytes_, ms):
-        return {"ms": round(ms, 4), "alg_bytes": bytes_, "gbs": round(bytes_ / (ms * 1e-3) / 1e9, 1),
-                "frac_of_hbm_peak": round(bytes_ / (ms * 1e-3) / 1e9 / peak, 4)}
+    def gbs(bytes_, ms, per=1):
+        """ms: the mean (and, from time_events, the distribution) of one timed replay, which
+        holds `per` launches of the stage."""
+        t = float(ms) / per
+        out = {"ms": round(t, 4), "alg_bytes": bytes_, "gbs": round(bytes_ / (t * 1e-3) / 1e9, 1),
+               "frac_of_hbm_peak": round(bytes_ / (t * 1e-3) / 1e9 / peak, 4)}
+        if isinstance(ms, Times):
+            out.update({"ms_median": round(ms.median / per, 4), "ms_p10": round(ms.p10 / per, 4),
+                        "ms_p90": round(ms.p90 / per, 4)})
+        return out
 
     # FP8 dispatch (dsv3 shape)
     w = workloads.make("dsv3_fp8")
@@ -709,7 +735,7 @@ def extra_stages(ep, dev, args, flush, peak):
     probs = [prob] + [prob.clone() for _ in range(NB - 1)]
     stagings = [staging] + [torch.empty_like(staging) for _ in range(NB - 1)]
     ms8 = time_events(lambda: [ep.ep_restripe_prob(probs[i], M, stagings[i]) for i in range(NB)], n, flush, stream)
-    res["restripe_prob"] = gbs(2 * T * Nn * P * 4, ms8 / NB)
+    res["restripe_prob"] = gbs(2 * T * Nn * P * 4, ms8, per=NB)
     res["restripe_prob"].update({"timing": f"{NB} launches back to back on distinct buffers in one graph, per launch",
                                  "single_launch_ms": round(ms1, 4),
                                  "single_launch_gbs": round(2 * T * Nn * P * 4 / (ms1 * 1e-3) / 1e9, 1)})

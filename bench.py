@@ -902,7 +902,7 @@ def extra_stages(ep, dev, args, flush, peak):
 
 # --------------------------------------------------------------------------- profiling runs
 
-PROFILE_STAGES = ("step", "sustained", "restripe", "send", "fp8")
+PROFILE_STAGES = ("step", "sustained", "restripe", "send", "fp8", "decode")
 
 
 def profile_stage(name):
@@ -910,7 +910,9 @@ def profile_stage(name):
     program for ncu captures (no timing, no JSON line). step: the dsv3 layout, dispatch and
     combine; sustained: the dsv3 step on 8 distinct buffer sets back to back; restripe: the
     prob restripe (T=8192, 8 nodes, P=128); send: the dsv3 send phase of the split combine;
-    fp8: the dsv3 FP8 dispatch, then the FP8-input combine of its rows."""
+    fp8: the dsv3 FP8 dispatch, then the FP8-input combine of its rows; decode: the
+    low-latency dispatch + permute of a T=128 dsv3 batch, then its low-latency weighted
+    combine."""
     import combine_ep_get_05_gb300 as ep
 
     ep.build_library()
@@ -971,6 +973,21 @@ def profile_stage(name):
             ep.dispatch(x, topk, tw, lay, w.max_tokens, fp8=True, out=d)
             flush()
             ep.combine_fp8(d.recv_x, d.recv_scales, lay, w.max_tokens, out=out)
+    elif name == "decode":
+        w, x, topk, tw = load("dsv3", T=128)
+        E, R, T, H, k = w.E, w.R, w.T, w.H, w.k
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        eslot = torch.empty((T, k), dtype=torch.int32, device=dev)
+        ews = torch.zeros(ep.ep_expert_layout_workspace_size(T, E), dtype=torch.uint8, device=dev)
+        ep.ep_get_expert_layout(topk, E, off, eslot, ews)
+        offs = off.cpu().numpy()
+        Mp = int(max(offs[(r + 1) * (E // R)] - offs[r * (E // R)] for r in range(R)))
+        px = torch.empty((R, Mp, H), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            flush()
+            ep.ep_dispatch_permuted_ll(x, topk, tw, E, R, Mp, off, eslot, px)
+            ep.ep_combine_permuted_ll(px, topk, tw, off, eslot, E, out)
     else:
         raise ValueError(f"unknown stage {name!r}; expected one of {PROFILE_STAGES}")
     torch.cuda.synchronize()

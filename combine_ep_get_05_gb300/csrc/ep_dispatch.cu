@@ -32,6 +32,11 @@ constexpr int kUnroll = 8;     // 16-byte vectors in flight per lane (bf16 path)
 constexpr int kRegDest = 8;    // destinations whose row offsets a warp keeps in registers
 constexpr int kUnrollFp8 = 2;  // warp iterations (4 blocks of 128 each) in flight (FP8 path)
 constexpr uint32_t kFp8BulkMaxSmem = 52 * 1024;  // shared memory of the bulk FP8 kernel (4 CTAs per SM)
+constexpr int kFp8Stages = 3;  // staging rows of the bulk FP8 kernel
+// roles of the bulk FP8 kernel's warps: 0-5 quantise, 6 writes scale rows, 7 lists tokens
+constexpr int kQuantWarps = 6;
+constexpr int kScaleWarp = 6;
+constexpr int kListWarp = 7;
 
 struct DispatchArgs {
     const uint16_t* x;
@@ -315,24 +320,24 @@ __global__ void __launch_bounds__(kThreads) dispatch_fp8_kernel(DispatchArgs a, 
 }
 
 // FP8 dispatch through shared memory and bulk copies: a CTA of 8 warps takes one token at a
-// time (tokens blockIdx.x, +gridDim.x, ...). Thread 0 streams the tokens' bf16 rows into two
-// shared-memory row buffers with bulk global->shared copies (two tokens ahead, completing on
-// mbarriers); for each token the 8 warps quantise the row from shared memory -- 8 lanes per
-// 128-element block, the quantiser of the register kernel -- into a staging code row (H
-// bytes) and scale row (H/128 floats) in shared memory; thread 0 sends the code row to every
-// destination with one bulk shared->global copy, and warp 0 writes the small scale rows with
-// 16-byte stores. The staging rows are double-buffered:
-// a token writes the buffer its predecessor's predecessor used once those stores have read
-// it, so the stores of one token overlap the quantisation of the next. No code passes
-// through a store from registers; the SM's work per byte is the quantiser's. Warp 0 resolves
-// each token's destinations and writes its metadata, from the slot row, ids and weights it
-// loaded into registers while the previous token was quantised. Every barrier wait is bounded; on
-// timeout the CTA waits (bounded) for its loads in flight, raises EP_FLAG_TIMEOUT and stops.
-// Used when H % 512 == 0 (scale rows of whole 16-byte vectors) and the buffers fit.
+// time (tokens blockIdx.x, +gridDim.x, ...). Every thread copies its 16-byte pieces of the
+// tokens' bf16 rows into two shared-memory row buffers by asynchronous copies, two tokens
+// ahead (these go through the load path, so they do not queue behind the CTA's bulk
+// stores). The warps have roles: warps 0-5 quantise the row from shared memory -- 8 lanes
+// per 128-element block, the quantiser of the register kernel -- into a staging code row (H
+// bytes) and scale row (H/128 floats); meanwhile warp 7 resolves the next token's
+// destinations and writes its metadata rows (from the slot row, ids and weights it loaded
+// into registers a token earlier) and warp 6 writes the previous token's scale rows with
+// 16-byte stores. After the CTA barrier thread 0 sends the code row to every destination
+// with one bulk shared->global copy. The staging rows form a ring of three and the
+// destination lists one of three (tokens i - 1, i, i + 1), so the stores of two tokens drain
+// while the next is quantised. No code passes through a store from registers. All waits
+// are hardware waits on the CTA's own copies (no spinning). Used when H % 512 == 0 (scale
+// rows of whole 16-byte vectors) and the buffers fit.
 struct Fp8Smem {
     uint32_t row_bytes, code_bytes, scale_bytes;
     uint32_t row_stride;    // row buffer b at b * row_stride
-    uint32_t stage_base;    // staging buffer b at stage_base + b * stage_stride: codes, then scales
+    uint32_t stage_base;    // staging buffer s at stage_base + s * stage_stride: codes, then scales
     uint32_t stage_stride;
     uint32_t scale_off;     // scales within a staging buffer
     uint32_t total;
@@ -348,16 +353,26 @@ inline Fp8Smem fp8_smem_layout(int H) {
     m.stage_base = 2u * m.row_stride;
     m.scale_off = up(m.code_bytes);
     m.stage_stride = m.scale_off + up(m.scale_bytes);
-    m.total = m.stage_base + 2u * m.stage_stride;
+    m.total = m.stage_base + kFp8Stages * m.stage_stride;
     return m;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ep::smem_addr(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 4) dispatch_fp8_bulk_kernel(DispatchArgs a, Fp8Smem m) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ __align__(8) uint64_t s_bar[2];
-    __shared__ int s_rank[kMaxDest];
-    __shared__ long long s_row[kMaxDest];
-    __shared__ int s_nd, s_ok;
+    // destination lists of three tokens (i - 1: its scale rows; i: quantised, its code rows;
+    // i + 1: being listed): row index r * max_tokens + slot (below 2^31) and rank
+    __shared__ int s_row[3][kMaxDest];
+    __shared__ uint8_t s_rank[3][kMaxDest];
+    __shared__ int s_nd[3];
     ep::grid_dependency_wait();  // dependent launch: inputs are ready after this
     const int tid = static_cast<int>(threadIdx.x);
     const int lane = tid & 31;
@@ -369,21 +384,21 @@ __global__ void __launch_bounds__(kThreads, 4) dispatch_fp8_bulk_kernel(Dispatch
     const int step = static_cast<int>(gridDim.x);
     const int n_my = first < a.T ? (a.T - 1 - first) / step + 1 : 0;
     uint8_t* recv = static_cast<uint8_t*>(a.recv_x);
-    int issued = 0;  // row loads issued by thread 0
-    if (tid == 0) {
-        ep::mbar_init(&s_bar[0], 1);
-        ep::mbar_init(&s_bar[1], 1);
-        ep::mbar_init_fence();
-        for (; issued < 2 && issued < n_my; ++issued) {
-            ep::mbar_arrive_expect_tx(&s_bar[issued], m.row_bytes);
-            ep::bulk_load(smem + issued * m.row_stride, a.x + static_cast<size_t>(first + issued * step) * a.H,
-                          m.row_bytes, &s_bar[issued]);
+    // row loads: every thread copies its 16-byte pieces of the token's bf16 row into row
+    // buffer q & 1, one commit group per token (empty past the last), two tokens ahead
+    const int nvec = a.H / 8;
+    auto load_row = [&](int q) {
+        if (q < n_my) {
+            const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(first + q * step) * a.H);
+            uint4* dst = reinterpret_cast<uint4*>(smem + (q & 1) * m.row_stride);
+            for (int v = tid; v < nvec; v += kThreads) cp_async16(dst + v, src + v);
         }
-        s_ok = 1;
-    }
-    __syncthreads();
-    // warp 0 holds the next token's slot row (lane r + 32c), top-k ids and weights (lane j)
-    // in registers, loaded a token ahead so that their latency hides behind a quantisation
+        cp_async_commit();
+    };
+    auto stage_of = [&](int q) { return smem + m.stage_base + (q % kFp8Stages) * m.stage_stride; };
+
+    // the listing warp holds a token's slot row (lane r + 32c), top-k ids and weights (lane j)
+    // in registers, loaded a token before it lists that token
     int sv[kMaxDest / 32];
     long long idv = -1;
     float wv = 0.0f;
@@ -396,107 +411,104 @@ __global__ void __launch_bounds__(kThreads, 4) dispatch_fp8_bulk_kernel(Dispatch
         idv = lane < a.k ? a.topk_idx[static_cast<size_t>(t) * a.k + lane] : -1;
         wv = (lane < a.k && a.recv_topk_w != nullptr) ? a.topk_w[static_cast<size_t>(t) * a.k + lane] : 0.0f;
     };
-    if (warp == 0 && n_my > 0) fetch_meta(first);
-    int i = 0;
-    for (; i < n_my; ++i) {
-        const int t = first + i * step;
-        const int b = i & 1;
-        if (warp == 0) {
-            // destinations of token t (ascending rank; slots >= max_tokens dropped)
-            int nd = 0;
-            bool over_any = false;
+    // list token t's destinations (ascending rank; slots >= max_tokens dropped) into list
+    // set `ls` and write its metadata rows (lane j: slot j of every destination)
+    auto list_token = [&](int t, int ls) {
+        int nd = 0;
+        bool over_any = false;
 #pragma unroll
-            for (int c = 0; c < kMaxDest / 32; ++c) {
-                if (c * 32 >= a.R) break;
-                const int r = c * 32 + lane;
-                const int sl = sv[c];
-                const bool over = sl >= a.max_tokens;
-                over_any |= over;
-                const bool ok = r < a.R && sl >= 0 && !over;
-                const uint32_t msk = __ballot_sync(ep::kFullMask, ok);
-                if (ok) {
-                    const int p = nd + __popc(msk & ep::lanemask_lt());
-                    s_rank[p] = r;
-                    s_row[p] = static_cast<long long>(r) * a.max_tokens + sl;
-                }
-                nd += __popc(msk);
+        for (int c = 0; c < kMaxDest / 32; ++c) {
+            if (c * 32 >= a.R) break;
+            const int r = c * 32 + lane;
+            const int sl = sv[c];
+            const bool over = sl >= a.max_tokens;
+            over_any |= over;
+            const bool ok = r < a.R && sl >= 0 && !over;
+            const uint32_t msk = __ballot_sync(ep::kFullMask, ok);
+            if (ok) {
+                const int p = nd + __popc(msk & ep::lanemask_lt());
+                s_rank[ls][p] = static_cast<uint8_t>(r);
+                s_row[ls][p] = r * a.max_tokens + sl;
             }
-            if (__any_sync(ep::kFullMask, over_any) && lane == 0) ep::raise_flag(a.status, EP_FLAG_CAPACITY);
-            if (__any_sync(ep::kFullMask, idv >= a.E) && lane == 0) ep::raise_flag(a.status, EP_FLAG_BAD_EXPERT);
-            __syncwarp();
-            // metadata: lane j writes slot j of every destination's rows
-            for (int d = 0; d < nd; ++d) {
-                const int r = s_rank[d];
-                const size_t row = static_cast<size_t>(s_row[d]);
-                if (lane == 0 && a.recv_src_idx != nullptr) a.recv_src_idx[row] = t;
-                if (lane < a.k) {
-                    const bool on = idv >= 0 && idv < a.E && static_cast<int>(idv) / a.epr == r;
-                    if (a.recv_topk_idx != nullptr)
-                        a.recv_topk_idx[row * a.k + lane] = on ? static_cast<int32_t>(idv) - r * a.epr : -1;
-                    if (a.recv_topk_w != nullptr) a.recv_topk_w[row * a.k + lane] = on ? wv : 0.0f;
-                }
-            }
-            if (i + 1 < n_my) fetch_meta(t + step);
-            if (lane == 0) {
-                s_nd = nd;
-                // staging buffer b was read by the stores of token i - 2: all but the newest
-                // bulk group (token i - 1) must have finished reading
-                ep::bulk_wait_read<1>();
-                if (!ep::mbar_wait_bounded(&s_bar[b], static_cast<uint32_t>((i >> 1) & 1))) s_ok = 0;
+            nd += __popc(msk);
+        }
+        if (__any_sync(ep::kFullMask, over_any) && lane == 0) ep::raise_flag(a.status, EP_FLAG_CAPACITY);
+        if (__any_sync(ep::kFullMask, idv >= a.E) && lane == 0) ep::raise_flag(a.status, EP_FLAG_BAD_EXPERT);
+        __syncwarp();
+        for (int d = 0; d < nd; ++d) {
+            const int r = s_rank[ls][d];
+            const size_t row = static_cast<size_t>(s_row[ls][d]);
+            if (lane == 0 && a.recv_src_idx != nullptr) a.recv_src_idx[row] = t;
+            if (lane < a.k) {
+                const bool on = idv >= 0 && idv < a.E && static_cast<int>(idv) / a.epr == r;
+                if (a.recv_topk_idx != nullptr)
+                    a.recv_topk_idx[row * a.k + lane] = on ? static_cast<int32_t>(idv) - r * a.epr : -1;
+                if (a.recv_topk_w != nullptr) a.recv_topk_w[row * a.k + lane] = on ? wv : 0.0f;
             }
         }
-        __syncthreads();
-        if (!s_ok) break;
-        const int nd = s_nd;
-        const uint16_t* row = reinterpret_cast<const uint16_t*>(smem + b * m.row_stride);
-        uint8_t* codes = smem + m.stage_base + b * m.stage_stride;
-        float* scales = reinterpret_cast<float*>(codes + m.scale_off);
-        if (nd > 0) {
-            // thread 0 saw the row's barrier complete; every reader observes that phase too
-            (void)ep::mbar_wait_bounded(&s_bar[b], static_cast<uint32_t>((i >> 1) & 1));
-            // a warp's 4 blocks are all in range or all out of it (nblk % 4 == 0), so the
-            // quantiser's shuffles always run on whole warps
-            for (int blk = warp * 4 + grp; blk < nblk; blk += kWarps * 4) {
-                const uint4* src = reinterpret_cast<const uint4*>(row + blk * 128 + pos * 16);
-                uint4 q;
-                float sc;
-                quantize16(src[0], src[1], q, sc);
-                *reinterpret_cast<uint4*>(codes + blk * 128 + pos * 16) = q;
-                if (pos == 0) scales[blk] = sc;
-            }
-            ep::fence_proxy_async_smem();
+        if (lane == 0) s_nd[ls] = nd;
+    };
+    // token q's scale rows: 16 bytes per lane, one store instruction per destination
+    auto store_scales = [&](int q) {
+        const int ls = q % 3;
+        const float* scales = reinterpret_cast<const float*>(stage_of(q) + m.scale_off);
+        for (int d = 0; d < s_nd[ls]; ++d) {
+            float* dsc = a.recv_scales + static_cast<size_t>(s_row[ls][d]) * nblk;
+            for (int v = lane; v < nblk / 4; v += 32)
+                ep::st_v4(dsc + 4 * v, *reinterpret_cast<const uint4*>(scales + 4 * v));
         }
-        __syncthreads();
-        if (warp == 0) {  // warp 0 also rewrites the destination list next token: program order
-            if (lane == 0) {
-                for (int d = 0; d < nd; ++d)
-                    ep::bulk_store(recv + static_cast<size_t>(s_row[d]) * a.H, codes, m.code_bytes);
-                ep::bulk_commit();
-                // row buffer b is free (every warp has quantised token i): token i + 2 goes there
-                if (issued < n_my) {
-                    ep::mbar_arrive_expect_tx(&s_bar[b], m.row_bytes);
-                    ep::bulk_load(smem + b * m.row_stride, a.x + static_cast<size_t>(first + issued * step) * a.H,
-                                  m.row_bytes, &s_bar[b]);
-                    ++issued;
+    };
+
+    load_row(0);
+    load_row(1);
+    if (warp == kListWarp && n_my > 0) {
+        fetch_meta(first);
+        list_token(first, 0);
+        if (n_my > 1) fetch_meta(first + step);
+    }
+    for (int i = 0; i < n_my; ++i) {
+        const int t = first + i * step;
+        const int ls = i % 3;
+        cp_async_wait<1>();  // this thread's pieces of token i's row have landed
+        __syncthreads();     // ... everyone's, token i listed, its staging buffer free
+        const int nd = s_nd[ls];
+        uint8_t* codes = stage_of(i);
+        if (warp < kQuantWarps) {
+            if (nd > 0) {
+                // a warp's 4 blocks are all in range or all out of it (nblk % 4 == 0), so the
+                // quantiser's shuffles always run on whole warps
+                const uint16_t* row = reinterpret_cast<const uint16_t*>(smem + (i & 1) * m.row_stride);
+                float* scales = reinterpret_cast<float*>(codes + m.scale_off);
+                for (int blk = warp * 4 + grp; blk < nblk; blk += kQuantWarps * 4) {
+                    const uint4* src = reinterpret_cast<const uint4*>(row + blk * 128 + pos * 16);
+                    uint4 q;
+                    float sc;
+                    quantize16(src[0], src[1], q, sc);
+                    *reinterpret_cast<uint4*>(codes + blk * 128 + pos * 16) = q;
+                    if (pos == 0) scales[blk] = sc;
                 }
+                ep::fence_proxy_async_smem();
             }
-            // the scale rows: 16 bytes per lane, one store instruction per destination
-            for (int d = 0; d < nd; ++d) {
-                float* dsc = a.recv_scales + static_cast<size_t>(s_row[d]) * nblk;
-                for (int v = lane; v < nblk / 4; v += 32)
-                    ep::st_v4(dsc + 4 * v, *reinterpret_cast<const uint4*>(scales + 4 * v));
-            }
+        } else if (warp == kScaleWarp) {
+            if (i > 0) store_scales(i - 1);
+        } else if (i + 1 < n_my) {  // the listing warp: the next token
+            list_token(t + step, (i + 1) % 3);
+            if (i + 2 < n_my) fetch_meta(t + 2 * step);
+        }
+        __syncthreads();  // token i quantised, token i + 1 listed
+        load_row(i + 2);  // row buffer i & 1 is free
+        if (tid == 0) {
+            for (int d = 0; d < nd; ++d)
+                ep::bulk_store(recv + static_cast<size_t>(s_row[ls][d]) * a.H, codes, m.code_bytes);
+            ep::bulk_commit();
+            // token i + 1 goes into the staging buffer of token i + 1 - kFp8Stages: all but
+            // the newest kFp8Stages - 1 bulk groups (one per token) must have read theirs
+            ep::bulk_wait_read<kFp8Stages - 1>();
         }
     }
+    if (warp == kScaleWarp && n_my > 0) store_scales(n_my - 1);
     ep::allow_dependents();
-    if (tid == 0) {
-        if (!s_ok) {
-            for (int q = i; q < issued; ++q)  // row i timed out: wait (bounded) for every load in flight
-                (void)ep::mbar_wait_bounded(&s_bar[q & 1], static_cast<uint32_t>((q >> 1) & 1));
-            ep::raise_flag(a.status, EP_FLAG_TIMEOUT);
-        }
-        ep::bulk_wait_all();
-    }
+    if (tid == 0) ep::bulk_wait_all();
 }
 
 std::atomic<int> g_fp8_bulk_smem_set[ep::kMaxDevices];

@@ -726,46 +726,72 @@ struct CombineSendArgs {
     int T, H, k, E, R, max_tokens, max_rows;
     uint16_t* y_rank;  // [R][max_tokens][H]
     int32_t* status;
+    float neg_zero;  // -0, passed at run time (see pair_add_product)
 };
 
+constexpr int kSendStages = 4;   // units in a warp's shared-memory ring: three in flight, one computed
+constexpr int kSendChunk = 128;  // 16-byte vectors of a row per unit: 4 per lane
 constexpr int kSendGroups = 4;  // 32-vector groups of a row a warp handles at once
 constexpr int kSendBatch = 2;   // sources loaded together
-constexpr int kSendWide = 8;    // groups in flight for a row with a single source
 constexpr int kSendRows = 32;   // rows a warp resolves at once (a lane per row)
 constexpr int kSendMaxSrc = 8;  // sources per row kept from that resolution
+
+// Per-lane asynchronous 16-byte copy global -> shared, issued only where `p` holds.
+__device__ __forceinline__ void send_cp_async16_if(void* smem, const void* gmem, bool p) {
+    asm volatile(
+        "{\n"
+        " .reg .pred q;\n"
+        " setp.ne.b32 q, %2, 0;\n"
+        " @q cp.async.cg.shared.global [%0], [%1], 16;\n"
+        "}" ::"r"(smem_addr(smem)),
+        "l"(gmem), "r"(static_cast<int>(p))
+        : "memory");
+}
+__device__ __forceinline__ void send_cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void send_cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// a0, a1 += RN(f0 * w), RN(f1 * w) on paired instructions with both roundings kept: the
+// product is a paired fused multiply-add with -0 (RN(f * w + -0) = RN(f * w) for every f
+// and w, zeros and their signs included), then a paired add. The -0 comes in at run time:
+// a plain paired multiply, or one with a constant zero, is contracted with the add into one
+// fused multiply-add (one rounding) by the code generator.
+__device__ __forceinline__ void pair_add_product(float& a0, float& a1, float f0, float f1, float w, float nz) {
+    asm("{\n"
+        " .reg .b64 f, s, z, p, a;\n"
+        " mov.b64 f, {%2, %3};\n"
+        " mov.b64 s, {%4, %4};\n"
+        " mov.b64 z, {%5, %5};\n"
+        " fma.rn.f32x2 p, f, s, z;\n"
+        " mov.b64 a, {%0, %1};\n"
+        " add.rn.f32x2 a, a, p;\n"
+        " mov.b64 {%0, %1}, a;\n"
+        "}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(f0), "f"(f1), "f"(w), "f"(nz));
+}
+// a0, a1 += f0, f1 on one paired add
+__device__ __forceinline__ void pair_add(float& a0, float& a1, float f0, float f1) {
+    asm("{\n"
+        " .reg .b64 f, a;\n"
+        " mov.b64 f, {%2, %3};\n"
+        " mov.b64 a, {%0, %1};\n"
+        " add.rn.f32x2 a, a, f;\n"
+        " mov.b64 {%0, %1}, a;\n"
+        "}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(f0), "f"(f1));
+}
 
 // Copies one rank-level row from its ns compacted sources (expert-major row offsets in
 // units of 16-byte vectors, weights), strictly in slot order: acc = 0, then per term one
 // fp32 multiply by the weight (when weighted) and one fp32 add, never fused; one rounding
 // to bf16 at the end.
 __device__ __forceinline__ void send_row(const CombineSendArgs& a, const uint4* ys, uint4* dst, int nvec, int ns,
-                                         const long long* srcs, const float* ws) {
+                                         const int* srcs, const float* ws) {
     const int lane = lane_id();
-    if (ns == 1) {
-        // one local expert (most rows): acc = 0 + term, kSendWide groups of loads in flight
-        const uint4* src1 = ys + srcs[0];
-        const float w = ws[0];
-        for (int v0 = lane; v0 < nvec; v0 += 32 * kSendWide) {
-            uint4 buf[kSendWide];
-#pragma unroll
-            for (int g = 0; g < kSendWide; ++g)
-                if (v0 + 32 * g < nvec) buf[g] = ld_stream_v4(src1 + v0 + 32 * g);
-#pragma unroll
-            for (int g = 0; g < kSendWide; ++g) {
-                if (v0 + 32 * g >= nvec) continue;
-                const uint32_t wd[4] = {buf[g].x, buf[g].y, buf[g].z, buf[g].w};
-                uint32_t o[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const float lo = a.recv_tw != nullptr ? __fmul_rn(bf16_lo(wd[h]), w) : bf16_lo(wd[h]);
-                    const float hi = a.recv_tw != nullptr ? __fmul_rn(bf16_hi(wd[h]), w) : bf16_hi(wd[h]);
-                    o[h] = pack_bf16x2_rn(__fadd_rn(0.0f, lo), __fadd_rn(0.0f, hi));
-                }
-                st_v4(dst + v0 + 32 * g, make_uint4(o[0], o[1], o[2], o[3]));
-            }
-        }
-        return;
-    }
     for (int v0 = lane; v0 < nvec; v0 += 32 * kSendGroups) {
         float acc[kSendGroups][8];
 #pragma unroll
@@ -778,7 +804,7 @@ __device__ __forceinline__ void send_row(const CombineSendArgs& a, const uint4* 
             for (int b = 0; b < kSendBatch; ++b)
 #pragma unroll
                 for (int g = 0; g < kSendGroups; ++g)
-                    if (d0 + b < ns && v0 + 32 * g < nvec) buf[b][g] = ld_stream_v4(ys + srcs[d0 + b] + v0 + 32 * g);
+                    if (d0 + b < ns && v0 + 32 * g < nvec) buf[b][g] = ld_stream_v4(ys + static_cast<size_t>(srcs[d0 + b]) * nvec + v0 + 32 * g);
 #pragma unroll
             for (int b = 0; b < kSendBatch; ++b) {
                 if (d0 + b >= ns) continue;
@@ -820,17 +846,22 @@ __device__ __forceinline__ void send_row(const CombineSendArgs& a, const uint4* 
 // so the dependent metadata loads of 32 rows overlap instead of running row after row.
 // Up to kSendMaxSrc sources per row are kept in shared memory, in slot order; a row with
 // more local experts is resolved again by the whole warp (lanes across slots) when its turn
-// comes. Phase 2 copies the batch's rows one after another (send_row).
+// comes and copied by send_row. Phase 2 streams the other rows of the batch through the
+// warp's shared-memory ring (stream_rows), so the loads of the next three units are in
+// flight while one is computed and occupy no registers.
 __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendArgs a) {
     grid_dependency_wait();  // dependent launch: the expert outputs are complete after this
-    __shared__ long long s_bsrc[kWarps][kSendRows][kSendMaxSrc];
+    // per batch row: its sources as expert-major row indices r * max_rows + p (below 2^31)
+    // with their weights, their number, the rank row r * max_tokens + s (below 2^31), token
+    __shared__ int s_bsrc[kWarps][kSendRows][kSendMaxSrc];
     __shared__ float s_bw[kWarps][kSendRows][kSendMaxSrc];
     __shared__ int s_bns[kWarps][kSendRows];
-    __shared__ long long s_brow[kWarps][kSendRows];
+    __shared__ int s_brow[kWarps][kSendRows];
     __shared__ int s_bt[kWarps][kSendRows];
-    __shared__ long long s_src[kWarps][kMaxTopk];
+    __shared__ int s_src[kWarps][kMaxTopk];
     __shared__ float s_w[kWarps][kMaxTopk];
     __shared__ int s_base[257];
+    extern __shared__ __align__(16) uint4 s_ring[];  // [kWarps][kSendStages][kSendChunk]
     const int lane = lane_id();
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int nvec = a.H / 8;
@@ -859,15 +890,123 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
     const int total = s_base[a.R];
     const uint4* ys = reinterpret_cast<const uint4*>(a.y_perm);
     uint4* outs = reinterpret_cast<uint4*>(a.y_rank);
-    // each warp owns a contiguous share of the rows, resolved up to kSendRows at a time
+    // phase 2's stream: units (row i of the batch, chunk c of kSendChunk vectors, source j)
+    // in order -- all sources of a chunk, then the next chunk, then the next row; a row
+    // without sources has one unit per chunk (zeros). The issuing side runs kSendStages - 1
+    // units ahead: each lane copies its 4 vectors of the unit into its own slots of the
+    // warp's ring (so no barrier between lanes is needed), and the arithmetic side reads
+    // them back. Per chunk: acc = +0, then acc += RN(x * w) (or x) in slot order, one
+    // rounding to bf16 at the end.
+    uint4* ring = s_ring + warp * (kSendStages * kSendChunk);
+    const int nchunks = (nvec + kSendChunk - 1) / kSendChunk;
+    const bool weighted = a.recv_tw != nullptr;
+    auto stream_rows = [&](int i0, int i1) {
+        // issuing side: unit (pi, pc, pj) of row pi with pns sources, the source's offset psrc
+        int pi = i0, pc = 0, pj = 0;
+        int pns = s_bns[warp][i0];
+        size_t psrc = pns > 0 ? static_cast<size_t>(s_bsrc[warp][i0][0]) * nvec : 0;
+        // arithmetic side: unit (ci, cc, cj) of row ci with cns sources, the source's weight cw
+        // and the row's output offset cout; the next unit's values are loaded a call ahead
+        int ci = i0, cc = 0, cj = 0;
+        int cns = pns;
+        float cw = pns > 0 ? s_bw[warp][i0][0] : 1.0f;
+        size_t cout = static_cast<size_t>(s_brow[warp][i0]) * nvec;
+        float acc[32];
+        auto produce = [&](int st) {
+            if (pi < i1) {
+                const int vb = pc * kSendChunk + lane;
+                if (pns > 0) {
+                    const uint4* src = ys + psrc + vb;
+                    uint4* dst = ring + st * kSendChunk + lane;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) send_cp_async16_if(dst + g * 32, src + g * 32, vb + g * 32 < nvec);
+                }
+                if (++pj < pns) {
+                    psrc = static_cast<size_t>(s_bsrc[warp][pi][pj]) * nvec;
+                } else {
+                    pj = 0;
+                    bool row_changed = false;
+                    if (++pc == nchunks) {
+                        pc = 0;
+                        row_changed = ++pi < i1;
+                        if (row_changed) pns = s_bns[warp][pi];
+                    }
+                    if ((row_changed || pns > 1) && pi < i1 && pns > 0)
+                        psrc = static_cast<size_t>(s_bsrc[warp][pi][0]) * nvec;
+                }
+            }
+            send_cp_async_commit();  // an empty group past the end keeps the waits uniform
+        };
+        auto consume = [&](int st) {
+            const int vb = cc * kSendChunk + lane;
+            if (cj == 0) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
+            }
+            if (cns > 0) {
+                const uint4* slot = ring + st * kSendChunk + lane;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (vb + g * 32 >= nvec) continue;
+                    const uint4 x = slot[g * 32];
+                    const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        float& a0 = acc[g * 8 + 2 * h];
+                        float& a1 = acc[g * 8 + 2 * h + 1];
+                        if (weighted) pair_add_product(a0, a1, bf16_lo(wd[h]), bf16_hi(wd[h]), cw, a.neg_zero);
+                        else pair_add(a0, a1, bf16_lo(wd[h]), bf16_hi(wd[h]));
+                    }
+                }
+            }
+            if (cj + 1 < cns) {
+                ++cj;
+                cw = s_bw[warp][ci][cj];
+                return;
+            }
+            // the chunk's last source: its bf16 vectors
+            uint4* dst = outs + cout + vb;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                if (vb + g * 32 >= nvec) continue;
+                uint4 o;
+                o.x = pack_bf16x2_rn(acc[g * 8 + 0], acc[g * 8 + 1]);
+                o.y = pack_bf16x2_rn(acc[g * 8 + 2], acc[g * 8 + 3]);
+                o.z = pack_bf16x2_rn(acc[g * 8 + 4], acc[g * 8 + 5]);
+                o.w = pack_bf16x2_rn(acc[g * 8 + 6], acc[g * 8 + 7]);
+                st_v4(dst + g * 32, o);
+            }
+            cj = 0;
+            if (++cc == nchunks) {
+                cc = 0;
+                if (++ci < i1) {
+                    cns = s_bns[warp][ci];
+                    cout = static_cast<size_t>(s_brow[warp][ci]) * nvec;
+                }
+            }
+            if (ci < i1 && cns > 0) cw = s_bw[warp][ci][0];
+        };
+#pragma unroll
+        for (int u = 0; u < kSendStages - 1; ++u) produce(u);
+        int st = 0;
+        while (ci < i1) {
+            produce(st == 0 ? kSendStages - 1 : st - 1);  // the stage consumed last step
+            send_cp_async_wait<kSendStages - 1>();
+            consume(st);
+            st = st + 1 == kSendStages ? 0 : st + 1;
+        }
+        send_cp_async_wait<0>();  // only empty groups can be left: nothing in flight on return
+    };
+
+    // warp gw of W takes the rows gw, gw + W, gw + 2W, ... (every SM then works on all
+    // ranks' rows alike), resolved up to kSendRows at a time: batch rows q0 + i * W
     const int nwarps = static_cast<int>(gridDim.x) * kWarps;
-    const int share = (total + nwarps - 1) / nwarps;
-    const int q_begin = (static_cast<int>(blockIdx.x) * kWarps + warp) * share;
-    const int q_end = q_begin + share < total ? q_begin + share : total;
-    for (int q0 = q_begin; q0 < q_end; q0 += kSendRows) {
-        const int nb = q_end - q0 < kSendRows ? q_end - q0 : kSendRows;
-        // phase 1: lane i resolves row q0 + i
-        const int q = q0 + lane;
+    const int gw = static_cast<int>(blockIdx.x) * kWarps + warp;
+    for (long long q0 = gw; q0 < total; q0 += static_cast<long long>(kSendRows) * nwarps) {
+        const long long left = (total - q0 + nwarps - 1) / nwarps;
+        const int nb = left < kSendRows ? static_cast<int>(left) : kSendRows;
+        // phase 1: lane i resolves row q0 + i * W
+        const int q = static_cast<int>(q0 + static_cast<long long>(lane) * nwarps);
         int n = 0, t = -1;
         bool over = false;
         long long orow = 0;
@@ -899,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
                             continue;
                         }
                         if (n < kSendMaxSrc) {
-                            s_bsrc[warp][lane][n] = (static_cast<long long>(r) * a.max_rows + p) * nvec;
+                            s_bsrc[warp][lane][n] = r * a.max_rows + p;
                             s_bw[warp][lane][n] = a.recv_tw != nullptr ? a.recv_tw[orow * a.k + j0 + i] : 1.0f;
                         }
                         ++n;
@@ -908,49 +1047,48 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
             }
         }
         s_bns[warp][lane] = n;
-        s_brow[warp][lane] = orow;
+        s_brow[warp][lane] = static_cast<int>(orow);
         s_bt[warp][lane] = t;
         if (__any_sync(kFullMask, over) && lane == 0) raise_flag(a.status, EP_FLAG_CAPACITY);
         __syncwarp();
-        // phase 2: the batch's rows
-        for (int i = 0; i < nb; ++i) {
-            int ns = s_bns[warp][i];
-            const long long row = s_brow[warp][i];
-            const long long* srcs = s_bsrc[warp][i];
-            const float* ws = s_bw[warp][i];
-            if (ns > kSendMaxSrc) {
-                // more local experts than phase 1 kept: lanes across slots, compacted by a ballot
-                const int r = static_cast<int>(row / a.max_tokens);
-                const int tt = s_bt[warp][i];
-                bool ok = false;
-                long long src = 0;
-                float wj = 1.0f;
-                if (lane < a.k) {
-                    const int l = a.recv_tidx[row * a.k + lane];
-                    const int32_t sl = a.eslot[static_cast<size_t>(tt) * a.k + lane];
-                    if (l >= 0 && l < epr && sl >= 0) {
-                        const int p = a.offsets[r * epr + l] - a.offsets[r * epr] + sl;
-                        if (p >= 0 && p < a.max_rows) {
-                            ok = true;
-                            src = (static_cast<long long>(r) * a.max_rows + p) * nvec;
-                            if (a.recv_tw != nullptr) wj = a.recv_tw[row * a.k + lane];
-                        }
+        // phase 2: runs of rows with at most kSendMaxSrc sources stream through the ring; a
+        // row with more is resolved again by the whole warp and copied on its own
+        for (int i = 0; i < nb;) {
+            int j = i;
+            while (j < nb && s_bns[warp][j] <= kSendMaxSrc) ++j;
+            if (j > i) stream_rows(i, j);
+            if (j == nb) break;
+            const long long row = s_brow[warp][j];  // the rank row r * max_tokens + s
+            // more local experts than phase 1 kept: lanes across slots, compacted by a ballot
+            const int r = static_cast<int>(row / a.max_tokens);
+            const int tt = s_bt[warp][j];
+            bool ok = false;
+            int src = 0;
+            float wj = 1.0f;
+            if (lane < a.k) {
+                const int l = a.recv_tidx[row * a.k + lane];
+                const int32_t sl = a.eslot[static_cast<size_t>(tt) * a.k + lane];
+                if (l >= 0 && l < epr && sl >= 0) {
+                    const int p = a.offsets[r * epr + l] - a.offsets[r * epr] + sl;
+                    if (p >= 0 && p < a.max_rows) {
+                        ok = true;
+                        src = r * a.max_rows + p;
+                        if (a.recv_tw != nullptr) wj = a.recv_tw[row * a.k + lane];
                     }
                 }
-                const uint32_t m = __ballot_sync(kFullMask, ok);
-                if (ok) {
-                    const int pos = __popc(m & lanemask_lt());
-                    s_src[warp][pos] = src;
-                    s_w[warp][pos] = wj;
-                }
-                __syncwarp();
-                ns = __popc(m);
-                srcs = s_src[warp];
-                ws = s_w[warp];
             }
-            send_row(a, ys, outs + row * nvec, nvec, ns, srcs, ws);
+            const uint32_t m = __ballot_sync(kFullMask, ok);
+            if (ok) {
+                const int pos = __popc(m & lanemask_lt());
+                s_src[warp][pos] = src;
+                s_w[warp][pos] = wj;
+            }
             __syncwarp();
+            send_row(a, ys, outs + row * nvec, nvec, __popc(m), s_src[warp], s_w[warp]);
+            __syncwarp();
+            i = j + 1;
         }
+        __syncwarp();  // the batch's lists are rewritten next
     }
     allow_dependents();
 }
@@ -1051,6 +1189,7 @@ __global__ void __launch_bounds__(kThreads) combine_permuted_ll_kernel(CombinePe
     }
 }
 
+std::atomic<int> g_send_smem_set[kMaxDevices];
 std::atomic<int> g_send_per_sm[kMaxDevices];
 
 std::atomic<int> g_ll_attr_set[kMaxDevices];
@@ -1220,16 +1359,19 @@ extern "C" ep_status_t ep_combine_send(const void* y_perm, const int32_t* recv_s
         return EP_ERR_INVALID;
     CombineSendArgs a{static_cast<const uint16_t*>(y_perm), recv_src_idx, recv_topk_idx, recv_topk_w, tokens_per_rank,
                       expert_offsets, expert_slot, T, H, k, E, R, max_tokens, max_rows,
-                      static_cast<uint16_t*>(y_rank), status};
+                      static_cast<uint16_t*>(y_rank), status, -0.0f};
+    constexpr int kRingBytes = kWarps * kSendStages * kSendChunk * 16;
+    ep_status_t occ = ensure_dynamic_smem(g_send_smem_set, combine_send_kernel, kRingBytes);
+    if (occ != EP_OK) return occ;
     int per_sm = 1;
-    const ep_status_t occ = blocks_per_sm(g_send_per_sm, combine_send_kernel, kThreads, 0, &per_sm);
+    occ = blocks_per_sm(g_send_per_sm, combine_send_kernel, kThreads, kRingBytes, &per_sm);
     if (occ != EP_OK) return occ;
     // rows received never exceed T per rank nor max_tokens
     const long long rows = static_cast<long long>(R) * (T < max_tokens ? T : max_tokens);
     const long long want = (rows + kWarps - 1) / kWarps;
     const long long cap = static_cast<long long>(sm_count()) * per_sm;
     const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
-    return launch_dependent(combine_send_kernel, dim3(grid), dim3(kThreads), 0, as_stream(stream), a);
+    return launch_dependent(combine_send_kernel, dim3(grid), dim3(kThreads), kRingBytes, as_stream(stream), a);
 }
 
 extern "C" ep_status_t ep_combine_permuted_ll(const void* y, const int64_t* topk_idx, const float* topk_w,

@@ -97,51 +97,19 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks)
 }
 
 // Combine of FP8 rows (E4M3 codes [R][max_tokens][H], one fp32 scale per 128 channels
-// [R][max_tokens][H/128]). Items are (token, 32 lanes x 16 channels); each warp takes a
-// contiguous run of its CTA's items. A warp walks its run in units of up to kUnitSrc
-// sources of one item and keeps two units in a shared-memory ring: while it computes one,
-// the next one's codes (16 per lane, one 16-byte vector) and block scales are on their way
-// by per-lane asynchronous copies, so the loads in flight occupy no registers. The
-// token's compacted source list (ascending rank) is built once per token, when the issuing
-// side reaches it, and only the issuing side reads it.
-// Per source a lane converts its 16 codes to fp32 exactly (E4M3 -> fp16 -> fp32 through
-// 16-bit register halves) and adds RN(code * scale) to its accumulators in source order,
-// two channels per instruction: the product as a paired fused multiply-add with -0
-// (RN(c * s + -0) = RN(c * s) for every c and s, zeros and their signs included), then a
-// paired add -- two roundings, as the definition has them. The -0 is a kernel argument: a
-// product written as a plain paired multiply, or with a constant zero, is contracted with
-// the following add into one fused multiply-add by the code generator (one rounding).
+// [R][max_tokens][H/128]). Items are (token, 32 lanes x 16 channels), taken by the warps in
+// runs of two strided over the batch (combine_fp8_kernel below). A warp walks its items in
+// units of up to kUnitSrc sources of one item and keeps two units in a shared-memory ring:
+// while it computes one, the next one's codes (16 per lane, one 16-byte vector) and block
+// scales are on their way by per-lane asynchronous copies, so the loads in flight occupy no
+// registers. Per source a lane converts its 16 codes to fp32 exactly (E4M3 -> fp16 -> fp32
+// through 16-bit register halves) and adds RN(code * scale) to its accumulators in source
+// order, two channels per instruction with both roundings kept (ep::pair_add_product, with
+// the -0 it needs passed in as a kernel argument).
 // The first term is taken as fma(code, scale, +0) = RN(code * scale + 0), one instruction
 // instead of two. It equals 0 + RN(code * scale) unless a nonzero product rounds to zero
 // (the fused form would keep a -0): with |code| >= 2^-9 that needs a scale below 2^-140,
 // so such scales (never produced by real data) take the two-instruction form.
-__device__ __forceinline__ void pair_add_product(float& a0, float& a1, float f0, float f1, float sc, float nz) {
-    asm("{\n"
-        " .reg .b64 f, s, z, p, a;\n"
-        " mov.b64 f, {%2, %3};\n"
-        " mov.b64 s, {%4, %4};\n"
-        " mov.b64 z, {%5, %5};\n"
-        " fma.rn.f32x2 p, f, s, z;\n"
-        " mov.b64 a, {%0, %1};\n"
-        " add.rn.f32x2 a, a, p;\n"
-        " mov.b64 {%0, %1}, a;\n"
-        "}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(f0), "f"(f1), "f"(sc), "f"(nz));
-}
-__device__ __forceinline__ void pair_first_product(float& a0, float& a1, float f0, float f1, float sc, float pz) {
-    asm("{\n"
-        " .reg .b64 f, s, z, a;\n"
-        " mov.b64 f, {%2, %3};\n"
-        " mov.b64 s, {%4, %4};\n"
-        " mov.b64 z, {%5, %5};\n"
-        " fma.rn.f32x2 a, f, s, z;\n"
-        " mov.b64 {%0, %1}, a;\n"
-        "}"
-        : "=f"(a0), "=f"(a1)
-        : "f"(f0), "f"(f1), "f"(sc), "f"(pz));
-}
-
 // zero: +0 for the first term's fused form, -0 for every later product
 template <bool kFirst>
 __device__ __forceinline__ void fp8_term16(float* acc, const uint4& v, float sc, float zero) {
@@ -152,8 +120,8 @@ __device__ __forceinline__ void fp8_term16(float* acc, const uint4& v, float sc,
         ep::e4m3x4_to_f32(w[q], f[0], f[1], f[2], f[3]);
 #pragma unroll
         for (int i = 0; i < 4; i += 2) {
-            if (kFirst) pair_first_product(acc[4 * q + i], acc[4 * q + i + 1], f[i], f[i + 1], sc, zero);
-            else pair_add_product(acc[4 * q + i], acc[4 * q + i + 1], f[i], f[i + 1], sc, zero);
+            if (kFirst) ep::pair_fma(acc[4 * q + i], acc[4 * q + i + 1], f[i], f[i + 1], sc, zero);
+            else ep::pair_add_product(acc[4 * q + i], acc[4 * q + i + 1], f[i], f[i + 1], sc, zero);
         }
     }
 }
@@ -161,32 +129,6 @@ __device__ __forceinline__ void fp8_term16(float* acc, const uint4& v, float sc,
 __device__ __forceinline__ bool fused_first_ok(float sc) { return sc == 0.0f || sc >= 0x1p-140f; }
 
 // Per-lane asynchronous copies, issued only where `p` holds (a predicate, not a branch).
-__device__ __forceinline__ void cp_async16_if(void* smem, const void* gmem, bool p) {
-    asm volatile(
-        "{\n"
-        " .reg .pred q;\n"
-        " setp.ne.b32 q, %2, 0;\n"
-        " @q cp.async.cg.shared.global [%0], [%1], 16;\n"
-        "}" ::"r"(ep::smem_addr(smem)),
-        "l"(gmem), "r"(static_cast<int>(p))
-        : "memory");
-}
-__device__ __forceinline__ void cp_async4_if(void* smem, const void* gmem, bool p) {
-    asm volatile(
-        "{\n"
-        " .reg .pred q;\n"
-        " setp.ne.b32 q, %2, 0;\n"
-        " @q cp.async.ca.shared.global [%0], [%1], 4;\n"
-        "}" ::"r"(ep::smem_addr(smem)),
-        "l"(gmem), "r"(static_cast<int>(p))
-        : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // one unit of the FP8 combine: up to kUnitSrc sources of item (t, lane vector v)
 struct Fp8Unit {
     int t, v, n;
@@ -296,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, kFp8CombineBlocks)
         // lane 4j + b copies the scale of the item's block b of source j
         const int sj = lane >> 2, sb = pg * 4 + (lane & 3);
         const unsigned srow = static_cast<unsigned>(list[pc + sj]);  // stale past n: never used
-        cp_async4_if(s_scale + st * L::kStageScales + lane, y_scales + static_cast<size_t>(srow) * nblk + sb,
+        ep::cp_async4_if(s_scale + st * L::kStageScales + lane, y_scales + static_cast<size_t>(srow) * nblk + sb,
                      sj < n && sb < nblk);
         if (v < nvec) {
             int rows[kUnitSrc];
@@ -313,10 +255,10 @@ __global__ void __launch_bounds__(kThreads, kFp8CombineBlocks)
 #pragma unroll
             for (int i = 0; i < kUnitSrc; ++i) {
                 // entries past n are stale list words: their addresses are formed, never used
-                cp_async16_if(dst + i * 32, src + static_cast<size_t>(static_cast<unsigned>(rows[i])) * nvec, i < n);
+                ep::cp_async16_if(dst + i * 32, src + static_cast<size_t>(static_cast<unsigned>(rows[i])) * nvec, i < n);
             }
         }
-        cp_async_commit();
+        ep::cp_async_commit();
         pc += n;
         if (u.last) {
             pc = 0;
@@ -391,8 +333,8 @@ __global__ void __launch_bounds__(kThreads, kFp8CombineBlocks)
     for (;;) {
         const bool more = pit < items;
         if (more) produce(st ^ 1, nxt);
-        else cp_async_commit();  // an empty group keeps the wait below uniform
-        cp_async_wait<1>();
+        else ep::cp_async_commit();  // an empty group keeps the wait below uniform
+        ep::cp_async_wait<1>();
         __syncwarp();
         consume(st, cur);
         if (!more) break;

@@ -289,4 +289,88 @@ __device__ __forceinline__ float f16_to_f32(uint32_t h) {
     return f;
 }
 
+
+// ---------------------------------------------------------------- per-thread async copies
+// global -> shared copies performed by the issuing thread in the background; a thread's
+// copies are grouped by commit and waited on by group count (a hardware wait, no spin)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+// issued only where `p` holds (a predicate, not a branch)
+__device__ __forceinline__ void cp_async16_if(void* smem, const void* gmem, bool p) {
+    asm volatile(
+        "{\n"
+        " .reg .pred q;\n"
+        " setp.ne.b32 q, %2, 0;\n"
+        " @q cp.async.cg.shared.global [%0], [%1], 16;\n"
+        "}" ::"r"(smem_addr(smem)),
+        "l"(gmem), "r"(static_cast<int>(p))
+        : "memory");
+}
+__device__ __forceinline__ void cp_async4_if(void* smem, const void* gmem, bool p) {
+    asm volatile(
+        "{\n"
+        " .reg .pred q;\n"
+        " setp.ne.b32 q, %2, 0;\n"
+        " @q cp.async.ca.shared.global [%0], [%1], 4;\n"
+        "}" ::"r"(smem_addr(smem)),
+        "l"(gmem), "r"(static_cast<int>(p))
+        : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// until at most N of the thread's newest groups are pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- paired fp32 arithmetic
+// Two channels per instruction with the roundings of the scalar definition. The product is
+// a paired fused multiply-add with a zero: RN(f * s + -0) = RN(f * s) for every f and s,
+// zeros and their signs included, so with nz = -0 it is the rounded product; the zero
+// comes in at run time because a plain paired multiply, or one with a constant zero, is
+// contracted with a following paired add into one fused multiply-add (one rounding) by the
+// code generator.
+
+// a0, a1 = RN(a0 + RN(f0 * s)), RN(a1 + RN(f1 * s)); nz = -0
+__device__ __forceinline__ void pair_add_product(float& a0, float& a1, float f0, float f1, float s, float nz) {
+    asm("{\n"
+        " .reg .b64 f, w, z, p, a;\n"
+        " mov.b64 f, {%2, %3};\n"
+        " mov.b64 w, {%4, %4};\n"
+        " mov.b64 z, {%5, %5};\n"
+        " fma.rn.f32x2 p, f, w, z;\n"
+        " mov.b64 a, {%0, %1};\n"
+        " add.rn.f32x2 a, a, p;\n"
+        " mov.b64 {%0, %1}, a;\n"
+        "}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(f0), "f"(f1), "f"(s), "f"(nz));
+}
+// a0, a1 = RN(f0 * s + z), RN(f1 * s + z), one rounding each
+__device__ __forceinline__ void pair_fma(float& a0, float& a1, float f0, float f1, float s, float z) {
+    asm("{\n"
+        " .reg .b64 f, w, y, a;\n"
+        " mov.b64 f, {%2, %3};\n"
+        " mov.b64 w, {%4, %4};\n"
+        " mov.b64 y, {%5, %5};\n"
+        " fma.rn.f32x2 a, f, w, y;\n"
+        " mov.b64 {%0, %1}, a;\n"
+        "}"
+        : "=f"(a0), "=f"(a1)
+        : "f"(f0), "f"(f1), "f"(s), "f"(z));
+}
+// a0, a1 = RN(a0 + f0), RN(a1 + f1)
+__device__ __forceinline__ void pair_add(float& a0, float& a1, float f0, float f1) {
+    asm("{\n"
+        " .reg .b64 f, a;\n"
+        " mov.b64 f, {%2, %3};\n"
+        " mov.b64 a, {%0, %1};\n"
+        " add.rn.f32x2 a, a, f;\n"
+        " mov.b64 {%0, %1}, a;\n"
+        "}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(f0), "f"(f1));
+}
+
 }  // namespace ep

@@ -357,15 +357,6 @@ inline Fp8Smem fp8_smem_layout(int H) {
     return m;
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ep::smem_addr(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 4) dispatch_fp8_bulk_kernel(DispatchArgs a, Fp8Smem m) {
     extern __shared__ __align__(128) unsigned char smem[];
     // destination lists of three tokens (i - 1: its scale rows; i: quantised, its code rows;
@@ -391,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 4) dispatch_fp8_bulk_kernel(Dispatch
         if (q < n_my) {
             const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(first + q * step) * a.H);
             uint4* dst = reinterpret_cast<uint4*>(smem + (q & 1) * m.row_stride);
-            for (int v = tid; v < nvec; v += kThreads) cp_async16(dst + v, src + v);
+            for (int v = tid; v < nvec; v += kThreads) ep::cp_async16(dst + v, src + v);
         }
-        cp_async_commit();
+        ep::cp_async_commit();
     };
     auto stage_of = [&](int q) { return smem + m.stage_base + (q % kFp8Stages) * m.stage_stride; };
 
@@ -469,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 4) dispatch_fp8_bulk_kernel(Dispatch
     for (int i = 0; i < n_my; ++i) {
         const int t = first + i * step;
         const int ls = i % 3;
-        cp_async_wait<1>();  // this thread's pieces of token i's row have landed
+        ep::cp_async_wait<1>();  // this thread's pieces of token i's row have landed
         __syncthreads();     // ... everyone's, token i listed, its staging buffer free
         const int nd = s_nd[ls];
         uint8_t* codes = stage_of(i);

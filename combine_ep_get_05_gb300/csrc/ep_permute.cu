@@ -726,7 +726,7 @@ struct CombineSendArgs {
     int T, H, k, E, R, max_tokens, max_rows;
     uint16_t* y_rank;  // [R][max_tokens][H]
     int32_t* status;
-    float neg_zero;  // -0, passed at run time (see pair_add_product)
+    float neg_zero;  // -0, passed at run time (see ep::pair_add_product)
 };
 
 constexpr int kSendStages = 4;   // units in a warp's shared-memory ring: three in flight, one computed
@@ -735,55 +735,6 @@ constexpr int kSendGroups = 4;  // 32-vector groups of a row a warp handles at o
 constexpr int kSendBatch = 2;   // sources loaded together
 constexpr int kSendRows = 32;   // rows a warp resolves at once (a lane per row)
 constexpr int kSendMaxSrc = 8;  // sources per row kept from that resolution
-
-// Per-lane asynchronous 16-byte copy global -> shared, issued only where `p` holds.
-__device__ __forceinline__ void send_cp_async16_if(void* smem, const void* gmem, bool p) {
-    asm volatile(
-        "{\n"
-        " .reg .pred q;\n"
-        " setp.ne.b32 q, %2, 0;\n"
-        " @q cp.async.cg.shared.global [%0], [%1], 16;\n"
-        "}" ::"r"(smem_addr(smem)),
-        "l"(gmem), "r"(static_cast<int>(p))
-        : "memory");
-}
-__device__ __forceinline__ void send_cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void send_cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// a0, a1 += RN(f0 * w), RN(f1 * w) on paired instructions with both roundings kept: the
-// product is a paired fused multiply-add with -0 (RN(f * w + -0) = RN(f * w) for every f
-// and w, zeros and their signs included), then a paired add. The -0 comes in at run time:
-// a plain paired multiply, or one with a constant zero, is contracted with the add into one
-// fused multiply-add (one rounding) by the code generator.
-__device__ __forceinline__ void pair_add_product(float& a0, float& a1, float f0, float f1, float w, float nz) {
-    asm("{\n"
-        " .reg .b64 f, s, z, p, a;\n"
-        " mov.b64 f, {%2, %3};\n"
-        " mov.b64 s, {%4, %4};\n"
-        " mov.b64 z, {%5, %5};\n"
-        " fma.rn.f32x2 p, f, s, z;\n"
-        " mov.b64 a, {%0, %1};\n"
-        " add.rn.f32x2 a, a, p;\n"
-        " mov.b64 {%0, %1}, a;\n"
-        "}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(f0), "f"(f1), "f"(w), "f"(nz));
-}
-// a0, a1 += f0, f1 on one paired add
-__device__ __forceinline__ void pair_add(float& a0, float& a1, float f0, float f1) {
-    asm("{\n"
-        " .reg .b64 f, a;\n"
-        " mov.b64 f, {%2, %3};\n"
-        " mov.b64 a, {%0, %1};\n"
-        " add.rn.f32x2 a, a, f;\n"
-        " mov.b64 {%0, %1}, a;\n"
-        "}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(f0), "f"(f1));
-}
 
 // Copies one rank-level row from its ns compacted sources (expert-major row offsets in
 // units of 16-byte vectors, weights), strictly in slot order: acc = 0, then per term one
@@ -919,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
                     const uint4* src = ys + psrc + vb;
                     uint4* dst = ring + st * kSendChunk + lane;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) send_cp_async16_if(dst + g * 32, src + g * 32, vb + g * 32 < nvec);
+                    for (int g = 0; g < 4; ++g) cp_async16_if(dst + g * 32, src + g * 32, vb + g * 32 < nvec);
                 }
                 if (++pj < pns) {
                     psrc = static_cast<size_t>(s_bsrc[warp][pi][pj]) * nvec;
@@ -935,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
                         psrc = static_cast<size_t>(s_bsrc[warp][pi][0]) * nvec;
                 }
             }
-            send_cp_async_commit();  // an empty group past the end keeps the waits uniform
+            cp_async_commit();  // an empty group past the end keeps the waits uniform
         };
         auto consume = [&](int st) {
             const int vb = cc * kSendChunk + lane;
@@ -991,11 +942,11 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
         int st = 0;
         while (ci < i1) {
             produce(st == 0 ? kSendStages - 1 : st - 1);  // the stage consumed last step
-            send_cp_async_wait<kSendStages - 1>();
+            cp_async_wait<kSendStages - 1>();
             consume(st);
             st = st + 1 == kSendStages ? 0 : st + 1;
         }
-        send_cp_async_wait<0>();  // only empty groups can be left: nothing in flight on return
+        cp_async_wait<0>();  // only empty groups can be left: nothing in flight on return
     };
 
     // warp gw of W takes the rows gw, gw + W, gw + 2W, ... (every SM then works on all

@@ -731,7 +731,7 @@ struct CombineSendArgs {
 
 constexpr int kSendStages = 4;   // units in a warp's shared-memory ring: three in flight, one computed
 constexpr int kSendChunk = 128;  // 16-byte vectors of a row per unit: 4 per lane
-constexpr int kSendGroups = 4;  // 32-vector groups of a row a warp handles at once
+constexpr int kSendGroups = 2;  // 32-vector groups of a row send_row handles at once
 constexpr int kSendBatch = 2;   // sources loaded together
 constexpr int kSendRows = 32;   // rows a warp resolves at once (a lane per row)
 constexpr int kSendMaxSrc = 8;  // sources per row kept from that resolution
@@ -800,6 +800,8 @@ __device__ __forceinline__ void send_row(const CombineSendArgs& a, const uint4* 
 // comes and copied by send_row. Phase 2 streams the other rows of the batch through the
 // warp's shared-memory ring (stream_rows), so the loads of the next three units are in
 // flight while one is computed and occupy no registers.
+// kWeighted: a.recv_tw != nullptr (terms multiplied by their weights)
+template <bool kWeighted>
 __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendArgs a) {
     grid_dependency_wait();  // dependent launch: the expert outputs are complete after this
     // per batch row: its sources as expert-major row indices r * max_rows + p (below 2^31)
@@ -850,7 +852,6 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
     // rounding to bf16 at the end.
     uint4* ring = s_ring + warp * (kSendStages * kSendChunk);
     const int nchunks = (nvec + kSendChunk - 1) / kSendChunk;
-    const bool weighted = a.recv_tw != nullptr;
     auto stream_rows = [&](int i0, int i1) {
         // issuing side: unit (pi, pc, pj) of row pi with pns sources, the source's offset psrc
         int pi = i0, pc = 0, pj = 0;
@@ -869,8 +870,13 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
                 if (pns > 0) {
                     const uint4* src = ys + psrc + vb;
                     uint4* dst = ring + st * kSendChunk + lane;
+                    if ((pc + 1) * kSendChunk <= nvec) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) cp_async16_if(dst + g * 32, src + g * 32, vb + g * 32 < nvec);
+                        for (int g = 0; g < 4; ++g) cp_async16(dst + g * 32, src + g * 32);
+                    } else {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) cp_async16_if(dst + g * 32, src + g * 32, vb + g * 32 < nvec);
+                    }
                 }
                 if (++pj < pns) {
                     psrc = static_cast<size_t>(s_bsrc[warp][pi][pj]) * nvec;
@@ -890,24 +896,30 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
         };
         auto consume = [&](int st) {
             const int vb = cc * kSendChunk + lane;
+            const bool full = (cc + 1) * kSendChunk <= nvec;  // all 4 of every lane's vectors in range
             if (cj == 0) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) acc[e] = 0.0f;
             }
+            auto add_vec = [&](int g, const uint4& x) {
+                const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    float& a0 = acc[g * 8 + 2 * h];
+                    float& a1 = acc[g * 8 + 2 * h + 1];
+                    if (kWeighted) pair_add_product(a0, a1, bf16_lo(wd[h]), bf16_hi(wd[h]), cw, a.neg_zero);
+                    else pair_add(a0, a1, bf16_lo(wd[h]), bf16_hi(wd[h]));
+                }
+            };
             if (cns > 0) {
                 const uint4* slot = ring + st * kSendChunk + lane;
+                if (full) {
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    if (vb + g * 32 >= nvec) continue;
-                    const uint4 x = slot[g * 32];
-                    const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+                    for (int g = 0; g < 4; ++g) add_vec(g, slot[g * 32]);
+                } else {
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        float& a0 = acc[g * 8 + 2 * h];
-                        float& a1 = acc[g * 8 + 2 * h + 1];
-                        if (weighted) pair_add_product(a0, a1, bf16_lo(wd[h]), bf16_hi(wd[h]), cw, a.neg_zero);
-                        else pair_add(a0, a1, bf16_lo(wd[h]), bf16_hi(wd[h]));
-                    }
+                    for (int g = 0; g < 4; ++g)
+                        if (vb + g * 32 < nvec) add_vec(g, slot[g * 32]);
                 }
             }
             if (cj + 1 < cns) {
@@ -917,15 +929,21 @@ __global__ void __launch_bounds__(kThreads, 2) combine_send_kernel(CombineSendAr
             }
             // the chunk's last source: its bf16 vectors
             uint4* dst = outs + cout + vb;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                if (vb + g * 32 >= nvec) continue;
+            auto put = [&](int g) {
                 uint4 o;
                 o.x = pack_bf16x2_rn(acc[g * 8 + 0], acc[g * 8 + 1]);
                 o.y = pack_bf16x2_rn(acc[g * 8 + 2], acc[g * 8 + 3]);
                 o.z = pack_bf16x2_rn(acc[g * 8 + 4], acc[g * 8 + 5]);
                 o.w = pack_bf16x2_rn(acc[g * 8 + 6], acc[g * 8 + 7]);
                 st_v4(dst + g * 32, o);
+            };
+            if (full) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) put(g);
+            } else {
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    if (vb + g * 32 < nvec) put(g);
             }
             cj = 0;
             if (++cc == nchunks) {
@@ -1141,7 +1159,9 @@ __global__ void __launch_bounds__(kThreads) combine_permuted_ll_kernel(CombinePe
 }
 
 std::atomic<int> g_send_smem_set[kMaxDevices];
+std::atomic<int> g_send_smem_set_w[kMaxDevices];
 std::atomic<int> g_send_per_sm[kMaxDevices];
+std::atomic<int> g_send_per_sm_w[kMaxDevices];
 
 std::atomic<int> g_ll_attr_set[kMaxDevices];
 std::atomic<int> g_attr_set[kMaxDevices];
@@ -1312,17 +1332,20 @@ extern "C" ep_status_t ep_combine_send(const void* y_perm, const int32_t* recv_s
                       expert_offsets, expert_slot, T, H, k, E, R, max_tokens, max_rows,
                       static_cast<uint16_t*>(y_rank), status, -0.0f};
     constexpr int kRingBytes = kWarps * kSendStages * kSendChunk * 16;
-    ep_status_t occ = ensure_dynamic_smem(g_send_smem_set, combine_send_kernel, kRingBytes);
+    auto kernel = recv_topk_w != nullptr ? combine_send_kernel<true> : combine_send_kernel<false>;
+    ep_status_t occ = ensure_dynamic_smem(recv_topk_w != nullptr ? g_send_smem_set_w : g_send_smem_set, kernel,
+                                          kRingBytes);
     if (occ != EP_OK) return occ;
     int per_sm = 1;
-    occ = blocks_per_sm(g_send_per_sm, combine_send_kernel, kThreads, kRingBytes, &per_sm);
+    occ = blocks_per_sm(recv_topk_w != nullptr ? g_send_per_sm_w : g_send_per_sm, kernel, kThreads, kRingBytes,
+                        &per_sm);
     if (occ != EP_OK) return occ;
     // rows received never exceed T per rank nor max_tokens
     const long long rows = static_cast<long long>(R) * (T < max_tokens ? T : max_tokens);
     const long long want = (rows + kWarps - 1) / kWarps;
     const long long cap = static_cast<long long>(sm_count()) * per_sm;
     const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
-    return launch_dependent(combine_send_kernel, dim3(grid), dim3(kThreads), kRingBytes, as_stream(stream), a);
+    return launch_dependent(kernel, dim3(grid), dim3(kThreads), kRingBytes, as_stream(stream), a);
 }
 
 extern "C" ep_status_t ep_combine_permuted_ll(const void* y, const int64_t* topk_idx, const float* topk_w,

@@ -86,6 +86,37 @@ def test_combine_fp8_random_rows_match_oracle(T, H, R, M, cap):
     assert np.array_equal(got, ref)
 
 
+def test_combine_fp8_tiny_scales_and_many_ranks_match_oracle():
+    """Scales from 2^-150 to 2^-130 (the first term takes its two-instruction form below
+    2^-140), zero scales, products that round to +-0 or to subnormals, and R = 100 ranks
+    (slot entries past the first 64 are read as the list is built)."""
+    T, H, R = 300, 256, 100
+    rng = np.random.Generator(np.random.PCG64(4242))
+    slot = np.full((T, R), -1, np.int32)
+    cnt = [0] * R
+    for t in range(T):
+        for r in range(R):
+            if rng.random() < 0.12:
+                slot[t, r] = cnt[r]
+                cnt[r] += 1
+    M = max(cnt)
+    codes = rng.integers(0, 256, (R, M, H)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3F  # no NaN codes
+    codes[:, :, ::7] = 0x80  # -0 codes
+    scales = np.ldexp(1.0, rng.integers(-150, -129, (R, M, H // 128))).astype(np.float32)
+    scales *= rng.uniform(1.0, 2.0, scales.shape).astype(np.float32)
+    scales[rng.random(scales.shape) < 0.1] = 0.0
+    assert (scales[scales > 0] < 2.0 ** -140).any() and (scales >= 2.0 ** -140).any()
+    got, flags = _gpu_combine_fp8(torch.from_numpy(codes).cuda(), torch.from_numpy(scales).cuda(),
+                                  torch.from_numpy(slot).cuda(), M, T, H)
+    ref, rflags = oracle.combine_fp8(codes, scales, slot, M)
+    assert flags == rflags == 0
+    assert np.array_equal(got, ref)
+    # the data reaches both signed zeros (a negative fp32 sum below bf16's smallest
+    # subnormal rounds to -0) and bf16 subnormals
+    assert (ref == 0x0000).any() and (ref == 0x8000).any() and (((ref & 0x7F80) == 0) & ((ref & 0x7F) != 0)).any()
+
+
 @pytest.mark.parametrize("name,over", [
     ("dsv3", {"T": 1000, "H": 8}),
     ("restripe", {"T": 700, "H": 8}),  # empty (-1) slots

@@ -57,7 +57,9 @@ typedef int32_t ep_status_t;
 #define EP_FLAG_CAPACITY 1   /* a receive slot >= max_tokens was dropped ([PR #453] commit
                                 "Add assertion against too large recv token count", as a flag) */
 #define EP_FLAG_BAD_EXPERT 2 /* a topk_idx entry >= E was skipped */
-#define EP_FLAG_TIMEOUT 4    /* a bounded wait of the layout scan gave up */
+#define EP_FLAG_TIMEOUT 4    /* a bounded wait gave up: a layout scan's look-back, or a
+                                bulk-copy row load of a BF16 dispatch (its copy is then
+                                incomplete) */
 #define EP_FLAG_WORKSPACE 8  /* the layout workspace was not at rest: zero-fill it and call again */
 
 typedef int32_t ep_dtype_t;
@@ -186,7 +188,8 @@ ep_status_t ep_get_layout_noalloc(const int64_t* topk_idx, int32_t T, int32_t k,
  *   recv_src_idx  int32 [R][max_tokens]                     (nullable)
  *   recv_topk_idx int32 [R][max_tokens][k]                  (nullable)
  *   recv_topk_w   fp32 [R][max_tokens][k]                   (nullable)
- *   status        EP_FLAG_CAPACITY, EP_FLAG_BAD_EXPERT
+ *   status        EP_FLAG_CAPACITY, EP_FLAG_BAD_EXPERT; EP_FLAG_TIMEOUT (BF16, rows
+ *                 moved by bulk copies: a row load that never completed)
  */
 ep_status_t ep_dispatch(const void* x, ep_dtype_t out_dtype, const int64_t* topk_idx,
                         const float* topk_w, const int32_t* slot, int32_t T, int32_t H, int32_t k,
@@ -329,7 +332,8 @@ ep_status_t ep_get_expert_layout(const int64_t* topk_idx, int32_t T, int32_t k, 
  *   expert_offsets / expert_slot from ep_get_expert_layout;
  *   perm_x bf16 [R][max_rows][H]; perm_src int32 [R][max_rows] (nullable);
  *   perm_w fp32 [R][max_rows] (nullable; needs topk_w); R * max_rows < 2^31.
- * p >= max_rows is dropped with EP_FLAG_CAPACITY; other rows are not written. */
+ * p >= max_rows is dropped with EP_FLAG_CAPACITY; other rows are not written;
+ * EP_FLAG_TIMEOUT as for ep_dispatch (bulk-copy row loads). */
 ep_status_t ep_dispatch_permuted(const void* x, const int64_t* topk_idx, const float* topk_w,
                                  const int32_t* expert_offsets, const int32_t* expert_slot,
                                  int32_t T, int32_t H, int32_t k, int32_t E, int32_t R,

@@ -25,6 +25,7 @@ timing is bracketed by barriers and the max over ranks is reported.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -215,6 +216,24 @@ def max_over_ranks(world, value):
 
 # --------------------------------------------------------------------------- oracle (CPU) timing
 
+@contextlib.contextmanager
+def one_core():
+    """Pin the calling thread (the oracle runs single-threaded in it) to one host core while
+    it is timed, and restore its affinity afterwards. Yields the core's index, or None where
+    the platform has no affinity call."""
+    try:
+        old = os.sched_getaffinity(0)
+    except (AttributeError, OSError):
+        yield None
+        return
+    core = max(old)  # the highest allowed core: away from core 0's interrupt load
+    try:
+        os.sched_setaffinity(0, {core})
+        yield core
+    finally:
+        os.sched_setaffinity(0, old)
+
+
 def oracle_step_seconds(w, max_tokens, tokens):
     """One oracle step (layout -> dispatch -> identity combine) on the first `tokens` tokens."""
     import oracle
@@ -237,15 +256,16 @@ def cpu_baseline(w, budget_s=12.0, tokens=None):
     tokens = tokens or w.T
     N = w.num_nodes
     spent, steps, pairs = 0.0, 0, 0
-    while spent < budget_s and steps < 50:
-        dt, pairs = oracle_step_seconds(w, tokens, tokens)
-        spent += dt
-        steps += 1
+    with one_core() as core:
+        while spent < budget_s and steps < 50:
+            dt, pairs = oracle_step_seconds(w, tokens, tokens)
+            spent += dt
+            steps += 1
     b = step_bytes(tokens, w.H, w.k, w.E, w.R, N, pairs)
     total = sum(b.values())
     return {
         "value": round(total / (spent / steps) / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-        "host": host_cpu(),
+        "host": host_cpu(), "pinned_core": core,
         "sample": f"{steps} oracle steps (layout+dispatch+identity combine) on {tokens} of the {w.T} tokens, "
                   f"single-threaded C, {spent:.1f} s",
         "tokens_per_s": round(tokens / (spent / steps), 1),
@@ -282,6 +302,13 @@ def host_cpu():
 def oracle_stage_baselines():
     """The oracle (single-threaded C, one host core) on a bounded sample of each extra stage's
     workload, in the same unit (algorithmic GB/s by the same formulas, scaled to the sample)."""
+    with one_core() as core:
+        res = _oracle_stage_baselines()
+    res["pinned_core"] = core
+    return res
+
+
+def _oracle_stage_baselines():
     import oracle
 
     oracle.build()
@@ -1035,13 +1062,14 @@ def run_reference(args, world, rank):
     oracle.build()
     w = workloads.make("dsv3")
     tokens = w.T
-    for _ in range(args.warmup):
-        oracle_step_seconds(w, tokens, tokens)
     times = []
     pairs = 0
-    for _ in range(args.steps):
-        dt, pairs = oracle_step_seconds(w, tokens, tokens)
-        times.append(dt)
+    with one_core() as core:
+        for _ in range(args.warmup):
+            oracle_step_seconds(w, tokens, tokens)
+        for _ in range(args.steps):
+            dt, pairs = oracle_step_seconds(w, tokens, tokens)
+            times.append(dt)
     s = statistics.mean(times)
     b = step_bytes(tokens, w.H, w.k, w.E, w.R, w.num_nodes, pairs)
     value = sum(b.values()) / s / 1e9
@@ -1055,7 +1083,7 @@ def run_reference(args, world, rank):
                                "(8 nodes x 4), max_tokens=4096, identity expert"},
         "tokens_per_s": round(tokens / s, 1),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
-                         "host": host_cpu()},
+                         "host": host_cpu(), "pinned_core": core},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

@@ -961,7 +961,7 @@ def extra_stages(ep, dev, args, flush, peak):
 
 # --------------------------------------------------------------------------- profiling runs
 
-PROFILE_STAGES = ("step", "sustained", "restripe", "send", "fp8", "decode")
+PROFILE_STAGES = ("step", "sustained", "restripe", "send", "fp8", "decode", "nodes", "permuted", "skewed")
 
 
 def profile_stage(name):
@@ -971,7 +971,10 @@ def profile_stage(name):
     prob restripe (T=8192, 8 nodes, P=128); send: the dsv3 send phase of the split combine;
     fp8: the dsv3 FP8 dispatch, then the FP8-input combine of its rows; decode: the
     low-latency dispatch + permute of a T=128 dsv3 batch, then its low-latency weighted
-    combine."""
+    combine; nodes: the restripe, then the sparse and the dense node dispatch (T=8192,
+    H=7168, 8 nodes, P=128); permuted: the dsv3 expert layout, fused dispatch + permute,
+    receive-side permute and weighted combine from the expert-major slabs; skewed: the
+    skewed layout, dispatch and combine (T=16384, H=4096, R=64, max_tokens = hottest rank)."""
     import combine_ep_get_05_gb300 as ep
 
     ep.build_library()
@@ -1047,6 +1050,56 @@ def profile_stage(name):
             flush()
             ep.ep_dispatch_permuted_ll(x, topk, tw, E, R, Mp, off, eslot, px)
             ep.ep_combine_permuted_ll(px, topk, tw, off, eslot, E, out)
+    elif name == "nodes":
+        w, x, topk, tw = load("restripe")
+        lay = ep.get_layout(topk, w.E, w.R, w.ranks_per_node)
+        prob = torch.from_numpy(w.prob).to(dev)
+        Nn, M, P, H = w.num_nodes, w.max_tokens, w.prob.shape[2], w.H
+        staging = torch.empty((Nn, M, P), dtype=torch.float32, device=dev)
+        rx = torch.empty((Nn, M, H), dtype=torch.bfloat16, device=dev)
+        rp = torch.empty((Nn, M, P), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            flush()
+            ep.ep_restripe_prob(prob, M, staging)
+            for mode in (ep.NODES_SPARSE, ep.NODES_DENSE):
+                flush()
+                ep.ep_dispatch_nodes(x, staging, lay.is_token_in_node, Nn, M, w.chunk_tokens, mode, rx, rp)
+    elif name == "permuted":
+        w, x, topk, tw = load("dsv3")
+        E, R, T, H, k = w.E, w.R, w.T, w.H, w.k
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        eslot = torch.empty((T, k), dtype=torch.int32, device=dev)
+        ews = torch.zeros(ep.ep_expert_layout_workspace_size(T, E), dtype=torch.uint8, device=dev)
+        ep.ep_get_expert_layout(topk, E, off, eslot, ews)
+        offs = off.cpu().numpy()
+        Mp = int(max(offs[(r + 1) * (E // R)] - offs[r * (E // R)] for r in range(R)))
+        px = torch.empty((R, Mp, H), dtype=torch.bfloat16, device=dev)
+        ps = torch.empty((R, Mp), dtype=torch.int32, device=dev)
+        pw = torch.empty((R, Mp), dtype=torch.float32, device=dev)
+        lay = ep.get_layout(topk, E, R, w.ranks_per_node)
+        d = ep.dispatch(x, topk, tw, lay, w.max_tokens)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            flush()
+            ep.ep_get_expert_layout(topk, E, off, eslot, ews)
+            flush()
+            ep.ep_dispatch_permuted(x, topk, tw, off, eslot, E, R, Mp, px, ps, pw)
+            flush()
+            ep.ep_permute_received(d.recv_x, d.recv_src_idx, d.recv_topk_idx, d.recv_topk_w, lay.tokens_per_rank,
+                                   off, eslot, E, Mp, px, ps, pw)
+            flush()
+            ep.ep_combine_permuted(px, topk, tw, off, eslot, E, out)
+    elif name == "skewed":
+        w, x, topk, tw = load("skewed")
+        lay = ep.get_layout(topk, w.E, w.R, w.ranks_per_node)
+        M = int(lay.tokens_per_rank.max().item())
+        d = ep.alloc_dispatch(w.R, M, w.H, w.k, device=dev)
+        out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            flush()
+            ep.get_layout(topk, w.E, w.R, w.ranks_per_node, out=lay)
+            ep.dispatch(x, topk, tw, lay, M, out=d)
+            ep.combine(d.recv_x, lay, M, out=out)
     else:
         raise ValueError(f"unknown stage {name!r}; expected one of {PROFILE_STAGES}")
     torch.cuda.synchronize()

@@ -790,8 +790,9 @@ __device__ __forceinline__ void send_row(const CombineSendArgs& a, const uint4* 
     }
 }
 
-// Each warp owns a contiguous share of the received rows and takes it kSendRows rows at a
-// time. Phase 1, a lane per row: the row (r, s) is
+// Warp w of the W warps takes the received rows w, w + W, w + 2W, ... (rows strided over the
+// batch, so every SM works on all ranks' rows alike), kSendRows rows at a time. Phase 1, a
+// lane per row: the row (r, s) is
 // found from the prefix of the per-rank counts in shared memory (binary search), and its
 // local experts are resolved to expert-major rows -- received id, expert slot, offsets --
 // so the dependent metadata loads of 32 rows overlap instead of running row after row.

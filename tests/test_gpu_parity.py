@@ -102,6 +102,11 @@ def run_rank_path(w, max_tokens=None, full_compare=True):
     ("dsv3_fp8", {"T": 300, "H": 24576}),  # wide FP8 rows
     ("dsv3_fp8", {"T": 40, "H": 26624}),
     ("dsv3_fp8", {"T": 30, "H": 33024}),   # more than 256 blocks: scales stored per iteration
+    # the shared-memory FP8 kernel (H % 512 == 0) with fewer tokens than CTAs: one CTA with
+    # one token, a few CTAs with one token each, CTAs with one or two tokens
+    ("dsv3_fp8", {"T": 1, "H": 512}),
+    ("dsv3_fp8", {"T": 5, "H": 7168}),
+    ("dsv3_fp8", {"T": 700, "H": 2048}),
     ("dsv3", {"T": 40, "H": 36864}),       # bf16 rows too large for the bulk-copy scatter
     ("skewed", {"T": 2000, "H": 256}),
     ("restripe", {"T": 700, "H": 512}),
